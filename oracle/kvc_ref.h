@@ -1,0 +1,148 @@
+/*
+ * kvc_ref.h -- the CPU oracle of the decode-time KV-cache compression event.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, fp64 restatement of the
+ * method, written to check the CUDA library against.  Only the test suite,
+ * the smoke check and the CPU-baseline leg of the benchmark may call it; the
+ * product path never does.  It shares no code, header, table or constant with
+ * the CUDA library.
+ *
+ * Sources (page title, then section / equation):
+ *  [AMS]  "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning",
+ *         Method -- Key designs 1-4, the complete example, and the schedule
+ *         defaults under "Loss function / training strategy".
+ *  [RKV]  "RefreshKV: Updating Small KV Cache During Long-form Generation",
+ *         A2 Method details (max pooling of neighbouring scores before top-K),
+ *         A6 Appendix (SnapKV baseline settings: window 1, kernel 7).
+ *  [SKV]  "SkipKV: Selective Skipping of KV Generation and Storage for
+ *         Efficient Inference with Large Reasoning Models", A2 Method details,
+ *         token importance score (query window, GQA map g(i) = floor(i/n),
+ *         attention mask M).
+ *
+ * Conventions.  A "unit" is one (layer, sequence, KV head).  Arrays handed to
+ * the batched entry points are unit-major and compact: [U, ...].  bf16 data
+ * is passed as its raw 16-bit patterns (uint16_t).  Every cache has T slots;
+ * slots [0, pad) are left padding and never take part; slots [pad, T) are the
+ * n = T - pad valid positions.
+ *
+ * Parity pins: every step is pinned by tests/test_oracle_*.py against closed
+ * forms, library routines, brute force or the worked example of [AMS].
+ */
+#ifndef KVC_REF_H
+#define KVC_REF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int group;        /* G: query heads per KV head                         */
+  int head_dim;     /* d                                                  */
+  int window;       /* W: most recent decode queries                      */
+  int budget;       /* T_keep                                             */
+  int avg_pool;     /* odd kernel of the mass average pool (5)            */
+  int max_pool;     /* odd kernel of the score max pool (7)               */
+  float delta;      /* cumulative-mass step (0.1)                         */
+  int seg_min;      /* 16                                                 */
+  int seg_max;      /* 256                                                */
+  int q_min;        /* 1                                                  */
+  int n_sink;       /* 4                                                  */
+  int n_recent;     /* recent suffix kept                                 */
+  float lambda;     /* EMA decay of the credit (0.9)                      */
+  float beta;       /* weight of the current mass in the mix (0.9)        */
+  float eps;        /* mass floor (1e-6)                                  */
+  float softmax_scale; /* 0 => 1/sqrt(head_dim)                           */
+} kvc_ref_config;
+
+/* ---- per-unit steps, fp64 (for the pins) -------------------------------- */
+
+/* Step 1: attention usage of the cache by the W most recent queries of the
+ * GQA group, summed over queries and heads, unseen suffix entries filled with
+ * the window max.  q: [G*W*d] (query j of head h at q[(h*W+j)*d]), k: [T*d].
+ * a: [T] (0 on padding).  *fill_out receives the fill value (window max p). */
+void kvc_ref_usage(const double* q, const double* k, int G, int W, int d,
+                   int T, int pad, double scale, double* a, double* fill_out);
+
+/* Step 1 (score): s = max-pool of a over valid neighbours within kernel/2;
+ * padding slots get -inf. */
+void kvc_ref_maxpool(const double* a, int T, int pad, int kernel, double* s);
+
+/* Step 2 (pool): u = average pool of a over the valid range, zero outside it,
+ * always divided by the kernel size.  Padding slots get 0. */
+void kvc_ref_avgpool(const double* a, int T, int pad, int kernel, double* u);
+
+/* Step 2 (mass): m_i = (max(u_i,0)+eps) / sum_v (max(u_v,0)+eps) over valid
+ * slots; 0 on padding. */
+void kvc_ref_mass_normalize(const double* u, int T, int pad, double eps,
+                            double* m);
+
+/* Step 2 (credit): slots [pad+n_carry, T) are new and take c_in := m.
+ * c = lambda*c_in + (1-lambda)*m;  m_used = normalize(beta*m +
+ * (1-beta)*normalize(c)).  c_out and m_used are 0 on padding. */
+void kvc_ref_credit(const double* m, const double* c_in, int T, int pad,
+                    int n_carry, double lambda, double beta, double* c_out,
+                    double* m_used);
+
+/* Step 3 (boundaries before split/merge): the fixed-point thresholds and
+ * b_k = min{t in [1,n] : C(t) >= tau_k}.  Writes up to *n_b boundaries
+ * (k = 1..K) to b[]; returns K. */
+int kvc_ref_boundaries(const float* m_used, int T, int pad, float delta,
+                       int64_t* b, uint64_t* total_out);
+
+/* Step 3 (segments): raw segments from the boundaries, empty ones dropped,
+ * merge of short ones, split of long ones.  Starts are valid offsets
+ * (0 = first valid slot).  Returns the number of segments. */
+int kvc_ref_segments(const float* m_used, int T, int pad, float delta,
+                     int seg_min, int seg_max, int32_t* seg_start,
+                     int32_t* seg_len, uint64_t* seg_mass);
+
+/* Step 4 (quotas): exact-integer quotas summing to min(budget, n). */
+void kvc_ref_quotas(const int32_t* seg_len, const uint64_t* seg_mass,
+                    int n_seg, int budget_eff, int q_min, int32_t* quota);
+
+/* Step 5 (selection): kept absolute slots, ascending; returns n_kept. */
+int kvc_ref_select_unit(const float* score, int T, int pad,
+                        const int32_t* seg_start, const int32_t* seg_len,
+                        const int32_t* quota, int n_seg, int budget,
+                        int n_sink, int n_recent, int32_t* kept);
+
+/* ---- batched mirrors of the library entry points (compact [U,...]) ------ */
+
+/* Largest segment count a cache of T slots can produce: max(1, T/seg_min). */
+int kvc_ref_s_max(const kvc_ref_config* cfg, int T);
+
+/* Steps 1-2 for U units.  q: [U,G,W,d] bf16 bits; k: [U,T,d] bf16 bits;
+ * credit_in: [U,T]; pad, n_carry: [U].  Outputs [U,T] fp32 (rounded from
+ * fp64): m_used, score, post-EMA credit. */
+int kvc_ref_mass(const kvc_ref_config* cfg, int U, int T, const uint16_t* q,
+                 const uint16_t* k, const float* credit_in,
+                 const int32_t* pad, const int32_t* n_carry, float* mass,
+                 float* score, float* credit_post);
+
+/* Steps 3-4 for U units on the fp32 mass.  Outputs [U,S_max]: starts as
+ * ABSOLUTE slots, lengths, quotas; n_seg [U]. */
+int kvc_ref_segment_quota(const kvc_ref_config* cfg, int U, int T,
+                          const float* mass, const int32_t* pad,
+                          int32_t* seg_start, int32_t* seg_len,
+                          int32_t* quota, int32_t* n_seg);
+
+/* Step 5 for U units on the fp32 score.  kept_idx: [U,budget], -1 past
+ * n_kept; n_kept: [U]. */
+int kvc_ref_select(const kvc_ref_config* cfg, int U, int T, const float* score,
+                   const int32_t* pad, const int32_t* seg_start,
+                   const int32_t* seg_len, const int32_t* quota,
+                   const int32_t* n_seg, int32_t* kept_idx, int32_t* n_kept);
+
+/* Step 6 for U units: rows of k, v ([U,T,d] bf16 bits) and credit ([U,T]) at
+ * the kept slots; slots past n_kept are zero. */
+int kvc_ref_compact(const kvc_ref_config* cfg, int U, int T, const uint16_t* k,
+                    const uint16_t* v, const float* credit_post,
+                    const int32_t* kept_idx, const int32_t* n_kept,
+                    uint16_t* k_out, uint16_t* v_out, float* credit_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
