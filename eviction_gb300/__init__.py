@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) decode-time KV-cache compression event.
+
+The computation lives in ``libkvc.so`` (hand-written CUDA kernels behind a C ABI,
+declared in ``include/kvc.h``). ``eviction_gb300.kvc`` is a thin ctypes binding
+with the same entry-point names that takes torch tensors and passes their device
+pointers and the current CUDA stream. There is no CPU fallback: every call fails
+loudly if the library or a CUDA device is missing.
+"""
+from .kvc import (Config, Handle, KvcError, library_path, load_library, ENTRY_POINTS)  # noqa: F401
+
+__all__ = ["Config", "Handle", "KvcError", "library_path", "load_library", "ENTRY_POINTS"]

@@ -1,0 +1,386 @@
+// kvc_api.cu -- host side of the C ABI declared in include/kvc.h: argument
+// validation, the handle and its workspace, and the stage / event entry points
+// (each a fixed sequence of kernel launches on the caller's stream).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+size_t attention_usage_smem_bytes(int d, int R);
+size_t segment_smem_bytes(const kvc_config& c, int T);
+size_t select_smem_bytes(const kvc_config& c, int T);
+}  // namespace kvc
+
+namespace {
+
+constexpr int kMaxT = 65536;
+constexpr int kMaxRows = 4096;  // G*W query rows per unit
+
+int fail(kvc_handle* h, int code, const std::string& msg) {
+  if (h) h->last_error = msg;
+  return code;
+}
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+int validate_config(const kvc_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return KVC_ERR_ARG;
+  };
+  if (!c) return bad("config is null");
+  if (c->n_layers < 1 || c->batch < 1 || c->n_kv_heads < 1 || c->group < 1)
+    return bad("n_layers, batch, n_kv_heads and group must be >= 1");
+  if (c->window < 1 || c->budget < 1 || c->max_T < 1)
+    return bad("window, budget and max_T must be >= 1");
+  if (c->max_T > kMaxT) return bad("max_T must be <= 65536");
+  if (c->avg_pool < 1 || c->avg_pool % 2 == 0 || c->max_pool < 1 || c->max_pool % 2 == 0)
+    return bad("avg_pool and max_pool must be odd and >= 1");
+  if (!std::isfinite(c->delta) || static_cast<double>(c->delta) < 1.0 / 1024.0)
+    return bad("delta must be finite and >= 1/1024");
+  if (c->seg_min < 1 || c->seg_max < 2 * c->seg_min || c->seg_max < 16 || c->seg_max > 4096)
+    return bad("need 1 <= seg_min, 2*seg_min <= seg_max, 16 <= seg_max <= 4096");
+  if (c->q_min < 0 || c->n_sink < 0 || c->n_recent < 0)
+    return bad("q_min, n_sink and n_recent must be >= 0");
+  if (!(c->lambda >= 0.f && c->lambda <= 1.f) || !(c->beta >= 0.f && c->beta <= 1.f))
+    return bad("lambda and beta must lie in [0, 1]");
+  if (!(c->eps > 0.f) || !std::isfinite(c->eps)) return bad("eps must be finite and > 0");
+  if (!(c->softmax_scale >= 0.f) || !std::isfinite(c->softmax_scale))
+    return bad("softmax_scale must be finite and >= 0");
+  if (c->head_dim != 64 && c->head_dim != 128) {
+    *why = "head_dim must be 64 or 128";
+    return KVC_ERR_UNSUPPORTED;
+  }
+  const long long rows = static_cast<long long>(c->group) * c->window;
+  if (rows > kMaxRows) {
+    *why = "group * window must be <= 4096";
+    return KVC_ERR_UNSUPPORTED;
+  }
+  const long long units = static_cast<long long>(c->n_layers) * c->batch * c->n_kv_heads;
+  if (units * c->max_T >= (1ll << 31) || units * rows >= (1ll << 31)) {
+    *why = "units * max_T and units * group * window must be < 2^31";
+    return KVC_ERR_UNSUPPORTED;
+  }
+  return KVC_OK;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_T(kvc_handle* h, int T) {
+  if (T < 1 || T > h->cfg.max_T)
+    return fail(h, KVC_ERR_SHAPE, "T must lie in [1, max_T]");
+  return KVC_OK;
+}
+
+int cuda_fail(kvc_handle* h, cudaError_t e, const char* where) {
+  return fail(h, KVC_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define KVC_REQUIRE_PTR(p)                                                    \
+  do {                                                                        \
+    if (!(p)) return fail(h, KVC_ERR_ARG, "null pointer: " #p);               \
+    if (!aligned16(p)) return fail(h, KVC_ERR_ALIGN, "not 16-byte aligned: " #p); \
+  } while (0)
+
+float scale_log2_of(const kvc_config& c) {
+  const double s = c.softmax_scale > 0.f ? static_cast<double>(c.softmax_scale)
+                                         : 1.0 / std::sqrt(static_cast<double>(c.head_dim));
+  return static_cast<float>(s * 1.4426950408889634);
+}
+
+}  // namespace
+
+extern "C" {
+
+void kvc_default_config(kvc_config* c) {
+  if (!c) return;
+  std::memset(c, 0, sizeof(*c));
+  c->window = 128;
+  c->avg_pool = 5;
+  c->max_pool = 7;
+  c->delta = 0.1f;
+  c->seg_min = 16;
+  c->seg_max = 256;
+  c->q_min = 1;
+  c->n_sink = 4;
+  c->n_recent = 64;
+  c->lambda = 0.9f;
+  c->beta = 0.9f;
+  c->eps = 1e-6f;
+  c->softmax_scale = 0.f;
+}
+
+const char* kvc_status_string(int code) {
+  switch (code) {
+    case KVC_OK: return "KVC_OK";
+    case KVC_ERR_ARG: return "KVC_ERR_ARG";
+    case KVC_ERR_SHAPE: return "KVC_ERR_SHAPE";
+    case KVC_ERR_ALIGN: return "KVC_ERR_ALIGN";
+    case KVC_ERR_NOMEM: return "KVC_ERR_NOMEM";
+    case KVC_ERR_CUDA: return "KVC_ERR_CUDA";
+    case KVC_ERR_DEVICE: return "KVC_ERR_DEVICE";
+    case KVC_ERR_TIMEOUT: return "KVC_ERR_TIMEOUT";
+    case KVC_ERR_UNSUPPORTED: return "KVC_ERR_UNSUPPORTED";
+    default: return "KVC_ERR_UNKNOWN";
+  }
+}
+
+const char* kvc_last_error(const kvc_handle* h) {
+  return h ? h->last_error.c_str() : "null handle";
+}
+
+int kvc_create(const kvc_config* cfg, kvc_handle** out) {
+  if (!out) return KVC_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  int rc = validate_config(cfg, &why);
+  if (rc != KVC_OK) {
+    std::fprintf(stderr, "kvc_create: %s\n", why.c_str());
+    return rc;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KVC_ERR_DEVICE;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KVC_ERR_DEVICE;
+  }
+  if (prop.major != 10 || prop.minor != 3) {
+    std::fprintf(stderr, "kvc_create: device %d is sm_%d%d, this library is built for sm_103a\n",
+                 dev, prop.major, prop.minor);
+    return KVC_ERR_DEVICE;
+  }
+  kvc_handle* h = new (std::nothrow) kvc_handle();
+  if (!h) return KVC_ERR_NOMEM;
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  kvc::Dims& d = h->dims;
+  d.L = cfg->n_layers;
+  d.B = cfg->batch;
+  d.H = cfg->n_kv_heads;
+  d.G = cfg->group;
+  d.W = cfg->window;
+  d.d = cfg->head_dim;
+  d.R = d.G * d.W;
+  d.U = d.L * d.B * d.H;
+
+  // shared-memory needs must fit the device
+  const size_t smem_max = prop.sharedMemPerBlockOptin;
+  if (kvc::attention_usage_smem_bytes(d.d, d.R) > smem_max ||
+      kvc::segment_smem_bytes(*cfg, cfg->max_T) > smem_max - 16 * 1024 ||
+      kvc::select_smem_bytes(*cfg, cfg->max_T) > smem_max - 1024) {
+    delete h;
+    std::fprintf(stderr, "kvc_create: configuration needs more shared memory than the device has\n");
+    return KVC_ERR_UNSUPPORTED;
+  }
+
+  const size_t U = d.U, T = cfg->max_T, R = d.R;
+  const size_t S = kvc::s_max_of(*cfg, cfg->max_T);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  const size_t o_row = take(U * R * sizeof(float2));
+  const size_t o_use = take(U * T * 4);
+  const size_t o_mass = take(U * T * 4);
+  const size_t o_score = take(U * T * 4);
+  const size_t o_cp = take(U * T * 4);
+  const size_t o_ss = take(U * S * 4);
+  const size_t o_sl = take(U * S * 4);
+  const size_t o_q = take(U * S * 4);
+  const size_t o_ns = take(U * 4);
+  const size_t o_st = take(256);
+  void* base = nullptr;
+  if (cudaMalloc(&base, off) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return KVC_ERR_NOMEM;
+  }
+  if (cudaMemset(base, 0, off) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(base);
+    delete h;
+    return KVC_ERR_CUDA;
+  }
+  char* p = static_cast<char*>(base);
+  kvc::Workspace& w = h->ws;
+  w.base = base;
+  w.bytes = off;
+  w.rowstat = reinterpret_cast<float2*>(p + o_row);
+  w.usage = reinterpret_cast<float*>(p + o_use);
+  w.mass = reinterpret_cast<float*>(p + o_mass);
+  w.score = reinterpret_cast<float*>(p + o_score);
+  w.credit_post = reinterpret_cast<float*>(p + o_cp);
+  w.seg_start = reinterpret_cast<int32_t*>(p + o_ss);
+  w.seg_len = reinterpret_cast<int32_t*>(p + o_sl);
+  w.quota = reinterpret_cast<int32_t*>(p + o_q);
+  w.n_seg = reinterpret_cast<int32_t*>(p + o_ns);
+  w.status = reinterpret_cast<uint32_t*>(p + o_st);
+  *out = h;
+  return KVC_OK;
+}
+
+void kvc_destroy(kvc_handle* h) {
+  if (!h) return;
+  if (h->ws.base) {
+    cudaDeviceSynchronize();
+    cudaFree(h->ws.base);
+  }
+  delete h;
+}
+
+int kvc_stage_sizes(const kvc_handle* h, int T, int* s_max) {
+  if (!h || !s_max) return KVC_ERR_ARG;
+  if (T < 1 || T > h->cfg.max_T) return KVC_ERR_SHAPE;
+  *s_max = kvc::s_max_of(h->cfg, T);
+  return KVC_OK;
+}
+
+int kvc_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T,
+             const int32_t* pad, const int32_t* n_carry, const float* credit_in,
+             float* credit_post, float* mass, float* score, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  KVC_REQUIRE_PTR(q);
+  KVC_REQUIRE_PTR(k);
+  KVC_REQUIRE_PTR(pad);
+  KVC_REQUIRE_PTR(n_carry);
+  KVC_REQUIRE_PTR(credit_in);
+  KVC_REQUIRE_PTR(credit_post);
+  KVC_REQUIRE_PTR(mass);
+  KVC_REQUIRE_PTR(score);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kvc::UsageArgs a{q, k, pad, T, scale_log2_of(h->cfg)};
+  std::string err;
+  cudaError_t e = kvc::launch_attention_usage(h, a, s, &err);
+  if (e != cudaSuccess)
+    return err.empty() ? cuda_fail(h, e, "attention usage") : fail(h, KVC_ERR_CUDA, err);
+  e = kvc::launch_mass_post(h, T, pad, n_carry, credit_in, credit_post, mass, score, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "mass");
+  return KVC_OK;
+}
+
+int kvc_segment_quota(kvc_handle* h, const float* mass, int T, const int32_t* pad,
+                      int32_t* seg_start, int32_t* seg_len, int32_t* quota,
+                      int32_t* n_seg, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  KVC_REQUIRE_PTR(mass);
+  KVC_REQUIRE_PTR(pad);
+  KVC_REQUIRE_PTR(seg_start);
+  KVC_REQUIRE_PTR(seg_len);
+  KVC_REQUIRE_PTR(quota);
+  KVC_REQUIRE_PTR(n_seg);
+  cudaError_t e = kvc::launch_segment_quota(h, mass, T, pad, seg_start, seg_len, quota,
+                                            n_seg, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "segment_quota");
+  return KVC_OK;
+}
+
+int kvc_select(kvc_handle* h, const float* score, int T, const int32_t* pad,
+               const int32_t* seg_start, const int32_t* seg_len, const int32_t* quota,
+               const int32_t* n_seg, int32_t* kept_idx, int32_t* n_kept, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  KVC_REQUIRE_PTR(score);
+  KVC_REQUIRE_PTR(pad);
+  KVC_REQUIRE_PTR(seg_start);
+  KVC_REQUIRE_PTR(seg_len);
+  KVC_REQUIRE_PTR(quota);
+  KVC_REQUIRE_PTR(n_seg);
+  KVC_REQUIRE_PTR(kept_idx);
+  KVC_REQUIRE_PTR(n_kept);
+  cudaError_t e = kvc::launch_select(h, score, T, pad, seg_start, seg_len, quota, n_seg,
+                                     kept_idx, n_kept, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "select");
+  return KVC_OK;
+}
+
+int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
+                const float* credit_post, int T, const int32_t* kept_idx,
+                const int32_t* n_kept, uint16_t* k_out, uint16_t* v_out,
+                float* credit_out, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  KVC_REQUIRE_PTR(k);
+  KVC_REQUIRE_PTR(v);
+  KVC_REQUIRE_PTR(credit_post);
+  KVC_REQUIRE_PTR(kept_idx);
+  KVC_REQUIRE_PTR(n_kept);
+  KVC_REQUIRE_PTR(k_out);
+  KVC_REQUIRE_PTR(v_out);
+  KVC_REQUIRE_PTR(credit_out);
+  cudaError_t e = kvc::launch_compact(h, k, v, credit_post, T, kept_idx, n_kept, k_out,
+                                      v_out, credit_out, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "compact");
+  return KVC_OK;
+}
+
+int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+              int T, const int32_t* pad, const int32_t* n_carry, const float* credit_in,
+              uint16_t* k_out, uint16_t* v_out, float* credit_out, int32_t* kept_idx,
+              int32_t* n_kept, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  KVC_REQUIRE_PTR(q);
+  KVC_REQUIRE_PTR(k);
+  KVC_REQUIRE_PTR(v);
+  KVC_REQUIRE_PTR(pad);
+  KVC_REQUIRE_PTR(n_carry);
+  KVC_REQUIRE_PTR(credit_in);
+  KVC_REQUIRE_PTR(k_out);
+  KVC_REQUIRE_PTR(v_out);
+  KVC_REQUIRE_PTR(credit_out);
+  KVC_REQUIRE_PTR(kept_idx);
+  KVC_REQUIRE_PTR(n_kept);
+  const kvc::Workspace& w = h->ws;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kvc::UsageArgs a{q, k, pad, T, scale_log2_of(h->cfg)};
+  std::string err;
+  cudaError_t e = kvc::launch_attention_usage(h, a, s, &err);
+  if (e != cudaSuccess)
+    return err.empty() ? cuda_fail(h, e, "attention usage") : fail(h, KVC_ERR_CUDA, err);
+  e = kvc::launch_mass_post(h, T, pad, n_carry, credit_in, w.credit_post, w.mass, w.score, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "mass");
+  e = kvc::launch_segment_quota(h, w.mass, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "segment_quota");
+  e = kvc::launch_select(h, w.score, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg,
+                         kept_idx, n_kept, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "select");
+  e = kvc::launch_compact(h, k, v, w.credit_post, T, kept_idx, n_kept, k_out, v_out,
+                          credit_out, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "compact");
+  return KVC_OK;
+}
+
+int kvc_get_device_status(kvc_handle* h, uint32_t* bits, void* stream) {
+  if (!h || !bits) return KVC_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "status sync");
+  uint32_t v = 0;
+  e = cudaMemcpy(&v, h->ws.status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+  e = cudaMemset(h->ws.status, 0, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(h, e, "status clear");
+  *bits = v;
+  return v ? KVC_ERR_TIMEOUT : KVC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,289 @@
+// kvc_internal.cuh -- shared internals of the sm_103a compression-event library:
+// the handle, kernel launch declarations, and thin inline-PTX wrappers for
+// mbarrier, TMA (cp.async.bulk.tensor) and the 5th-generation tensor core
+// (tcgen05: TMEM allocation, MMA, commit, TMEM loads).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "kvc.h"
+
+namespace kvc {
+
+// ---------------------------------------------------------------- handle ----
+
+struct Workspace {
+  float2* rowstat = nullptr;    // [U][R]  {log2 normaliser b_r, 1/Z'_r}
+  float* usage = nullptr;       // [U][max_T] raw usage (no fill)
+  float* mass = nullptr;        // [U][max_T]   (event intermediates)
+  float* score = nullptr;       // [U][max_T]
+  float* credit_post = nullptr; // [U][max_T]
+  int32_t* seg_start = nullptr; // [U][S_max(max_T)]
+  int32_t* seg_len = nullptr;
+  int32_t* quota = nullptr;
+  int32_t* n_seg = nullptr;     // [U]
+  uint32_t* status = nullptr;   // device status bits
+  void* base = nullptr;         // single allocation
+  size_t bytes = 0;
+};
+
+struct Dims {
+  int L, B, H, G, W, d, R, U;  // R = G*W query rows per unit, U = L*B*H units
+};
+
+}  // namespace kvc
+
+struct kvc_handle {
+  kvc_config cfg;
+  kvc::Dims dims;
+  kvc::Workspace ws;
+  int device = 0;
+  int num_sms = 0;
+  std::string last_error;
+};
+
+namespace kvc {
+
+// ------------------------------------------------------------ launchers ----
+// All return cudaSuccess or the launch error.  Defined next to their kernels.
+
+struct UsageArgs {
+  const uint16_t* q;
+  const uint16_t* k;
+  const int32_t* pad;
+  int T;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+// Pass 1 + pass 2 of the window attention usage (tcgen05 kernels).
+cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a,
+                                   cudaStream_t s, std::string* err);
+
+cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
+                             const int32_t* n_carry, const float* credit_in,
+                             float* credit_post, float* mass, float* score,
+                             cudaStream_t s);
+
+cudaError_t launch_segment_quota(const kvc_handle* h, const float* mass, int T,
+                                 const int32_t* pad, int32_t* seg_start,
+                                 int32_t* seg_len, int32_t* quota,
+                                 int32_t* n_seg, cudaStream_t s);
+
+cudaError_t launch_select(const kvc_handle* h, const float* score, int T,
+                          const int32_t* pad, const int32_t* seg_start,
+                          const int32_t* seg_len, const int32_t* quota,
+                          const int32_t* n_seg, int32_t* kept_idx,
+                          int32_t* n_kept, cudaStream_t s);
+
+cudaError_t launch_compact(const kvc_handle* h, const uint16_t* k,
+                           const uint16_t* v, const float* credit_post, int T,
+                           const int32_t* kept_idx, const int32_t* n_kept,
+                           uint16_t* k_out, uint16_t* v_out,
+                           float* credit_out, cudaStream_t s);
+
+inline int s_max_of(const kvc_config& c, int T) {
+  int s = T / c.seg_min;
+  return s > 1 ? s : 1;
+}
+
+// ------------------------------------------------------ device helpers ----
+
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bound on any single wait of a pipeline role (ns).  Correct code waits
+// microseconds; the bound only exists so that a broken pipeline reports an
+// error instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar,
+                                                      uint32_t bytes) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// after kWaitLimitNs or as soon as *abort becomes non-zero; returns false then
+// (and on its own time-out raises *abort and the device status bit).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort,
+                                          uint32_t* status) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_test(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      atomicOr(status, KVC_STATUS_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// 2-D tiled TMA load global -> shared, completion on `bar` (transaction bytes).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
+                                            int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+
+// ---- tcgen05 ----
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile(
+      "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+          smem_u32(slot)),
+      "r"(ncols)
+      : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile(
+      "tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+      "r"(ncols)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core-matrix groups 1024 bytes apart.  `addr` must lie in a
+// 1024-byte aligned tile (plus the K-slice byte offset within the row).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t desc = 0;
+  desc |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);  // start address
+  desc |= static_cast<uint64_t>(1) << 16;                  // LBO (unused)
+  desc |= static_cast<uint64_t>(1024 >> 4) << 32;          // SBO
+  desc |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+  desc |= static_cast<uint64_t>(2) << 61;                  // SWIZZLE_128B
+  return desc;
+}
+
+// Instruction descriptor, kind::f16: A = B = bf16, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                                   // D format f32
+         | (1u << 7)                                 // A format bf16
+         | (1u << 10)                                // B format bf16
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc,
+                                         uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
+      "[%0];" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
+// (warp's lane quarter)*32 + i, columns col..col+31.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "[%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Hardware base-2 exponential (MUFU), flush-to-zero.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key).
+__device__ __forceinline__ uint32_t float_order_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+#endif  // __CUDACC__
+
+}  // namespace kvc

@@ -1,0 +1,197 @@
+// mass_post.cu -- from raw usage to score, mass and credit, one CTA per unit.
+//
+// "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning", Method,
+// Key design 1:
+//   * entries a window query cannot see (causal suffix) are filled with the
+//     window's maximum score: the largest softmax probability of the unit,
+//     max_r 1/Z'_r, taken from pass 1 of the attention kernel;
+//   * u = average pool (kernel avg_pool, zero outside the valid slots, divided
+//     by the kernel size);  m_i = (max(u_i,0)+eps) / sum_v (max(u_v,0)+eps);
+//   * c = lambda*c_in + (1-lambda)*m with c_in := m on slots that are new since
+//     the last event;  m_used = normalize(beta*m + (1-beta)*normalize(c)).
+// The base score ("RefreshKV: ...", A2: max pooling of neighbouring attention
+// scores; A6: kernel 7) is the filled usage max-pooled over valid neighbours.
+//
+// The unit's data (a few KB per array) stays in L1/L2 between the sweeps; each
+// sweep is a strided pass plus one block reduction (fixed order, so repeated
+// runs give identical bits).
+#include <cmath>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  __syncthreads();  // red may still be read by a previous reduction
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  if (threadIdx.x < 32) {
+    t = (lane < kThreads / 32) ? red[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) red[kThreads / 32] = t;
+  }
+  __syncthreads();
+  return red[kThreads / 32];
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float t = (lane < kThreads / 32) ? red[lane] : -INFINITY;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
+    if (lane == 0) red[kThreads / 32] = t;
+  }
+  __syncthreads();
+  return red[kThreads / 32];
+}
+
+struct PostParams {
+  int T, R, W, G, B, H;
+  int avg_pool, max_pool;
+  float eps, lambda, beta;
+  const float2* rowstat;
+  float* usage;  // raw usage, filled in place
+  const int32_t* pad;
+  const int32_t* n_carry;
+  const float* credit_in;
+  float* credit_post;
+  float* mass;
+  float* score;
+};
+
+__global__ void __launch_bounds__(kThreads)
+    mass_post_kernel(PostParams p) {
+  __shared__ float red[kThreads / 32 + 1];
+  const int u = blockIdx.x;
+  const int b = (u / p.H) % p.B;
+  const int T = p.T;
+  const int pad = min(max(p.pad[b], 0), T);
+  const size_t base = static_cast<size_t>(u) * T;
+  float* a = p.usage + base;
+  float* mass = p.mass + base;
+  float* score = p.score + base;
+  float* cpost = p.credit_post + base;
+  const float* cin = p.credit_in + base;
+
+  if (pad >= T) {
+    for (int i = threadIdx.x; i < T; i += kThreads) {
+      mass[i] = 0.f;
+      score[i] = -INFINITY;
+      cpost[i] = 0.f;
+    }
+    return;
+  }
+
+  // fill value = largest probability of any present row (absent rows hold 0)
+  float pm = 0.f;
+  for (int r = threadIdx.x; r < p.R; r += kThreads)
+    pm = fmaxf(pm, p.rowstat[static_cast<size_t>(u) * p.R + r].y);
+  const float fill = block_max(pm, red);
+
+  // a'(i) = a(i) + fill * (#present (head, query) pairs that cannot see i)
+  const int j_lo = max(0, pad - (T - p.W));  // first present window query
+  for (int i = pad + threadIdx.x; i < T; i += kThreads) {
+    const int unseen = max(0, min(p.W, i - T + p.W) - j_lo) * p.G;
+    if (unseen > 0) a[i] += fill * static_cast<float>(unseen);
+  }
+  __syncthreads();
+
+  // score = max-pooled usage; first mass total
+  const int ra = p.avg_pool / 2, rm = p.max_pool / 2;
+  const float inv_k = 1.0f / static_cast<float>(p.avg_pool);
+  float tot = 0.f;
+  for (int i = threadIdx.x; i < T; i += kThreads) {
+    if (i < pad) {
+      score[i] = -INFINITY;
+      continue;
+    }
+    float mx = -INFINITY;
+    for (int t = max(pad, i - rm); t <= min(T - 1, i + rm); ++t) mx = fmaxf(mx, a[t]);
+    score[i] = mx;
+    float s = 0.f;
+    for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
+    tot += fmaxf(s * inv_k, 0.f) + p.eps;
+  }
+  const float total1 = block_sum(tot, red);
+
+  // mass and credit
+  const int n_carry = min(max(p.n_carry[b], 0), T - pad);
+  const float lam = p.lambda;
+  float ctot = 0.f;
+  for (int i = threadIdx.x; i < T; i += kThreads) {
+    if (i < pad) {
+      mass[i] = 0.f;
+      cpost[i] = 0.f;
+      continue;
+    }
+    float s = 0.f;
+    for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
+    const float m = (fmaxf(s * inv_k, 0.f) + p.eps) / total1;
+    const float prior = (i < pad + n_carry) ? cin[i] : m;
+    const float c = lam * prior + (1.0f - lam) * m;
+    mass[i] = m;
+    cpost[i] = c;
+    ctot += c;
+  }
+  const float c_total = block_sum(ctot, red);
+
+  // mix and normalise
+  const float beta = p.beta;
+  float mtot = 0.f;
+  for (int i = pad + threadIdx.x; i < T; i += kThreads) {
+    const float m = mass[i];
+    const float cn = (c_total > 0.f) ? cpost[i] / c_total : m;
+    const float mix = beta * m + (1.0f - beta) * cn;
+    mass[i] = mix;
+    mtot += mix;
+  }
+  const float mix_total = block_sum(mtot, red);
+  for (int i = pad + threadIdx.x; i < T; i += kThreads) mass[i] = mass[i] / mix_total;
+}
+
+}  // namespace
+
+cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
+                             const int32_t* n_carry, const float* credit_in,
+                             float* credit_post, float* mass, float* score,
+                             cudaStream_t s) {
+  const Dims& dm = h->dims;
+  PostParams p;
+  p.T = T;
+  p.R = dm.R;
+  p.W = dm.W;
+  p.G = dm.G;
+  p.B = dm.B;
+  p.H = dm.H;
+  p.avg_pool = h->cfg.avg_pool;
+  p.max_pool = h->cfg.max_pool;
+  p.eps = h->cfg.eps;
+  p.lambda = h->cfg.lambda;
+  p.beta = h->cfg.beta;
+  p.rowstat = h->ws.rowstat;
+  p.usage = h->ws.usage;
+  p.pad = pad;
+  p.n_carry = n_carry;
+  p.credit_in = credit_in;
+  p.credit_post = credit_post;
+  p.mass = mass;
+  p.score = score;
+  mass_post_kernel<<<dm.U, kThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

@@ -1,0 +1,420 @@
+// segment_quota.cu -- cumulative-mass segmentation and segment quotas, one CTA
+// per unit, in exact integer arithmetic.
+//
+// "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning", Method:
+//  Key design 2:  C(t) = sum_{u<=t} m_u,  b_k = min{t | C(t) >= k*Delta};
+//                 segments longer than the maximum are split into near-equal
+//                 parts, short adjacent ones merged (16..256), masses recounted.
+//  Key design 3:  q_i^min = min(q_min, L_i), T_rem = T_keep - sum q_i^min,
+//                 q_i = q_i^min + round(T_rem M_i / sum M), clipped to L_i and
+//                 corrected to the exact budget.
+//
+// Exactness: the fp32 mass becomes 40-bit fixed point (mu = trunc(m * 2^40),
+// exact), prefix sums are uint64, the thresholds are
+// tau_k = ceil(fl(fl(k*Delta) * S)) in IEEE double with round-to-nearest and no
+// fused operations, the split/merge and quota rules are integer only.  The
+// same definitions with the same tie rules give the same bits on any machine.
+//   * empty raw segments are dropped; merge left to right until >= seg_min,
+//     a short tail joins its predecessor; then split L > seg_max into
+//     c = ceil(L/seg_max) parts, the first L mod c one longer;
+//   * budget = min(T_keep, n); infeasible minimums go to the heaviest segments
+//     (ties: lower index); round = half up; correction one unit at a time on the
+//     exact remainder (short: largest remainder among q < L, ties lower index;
+//     over: smallest remainder among q > q^min, ties higher index).
+#include <cmath>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxK = 1024;  // thresholds: delta >= 1/1024
+
+__device__ __forceinline__ uint64_t fixed_mass(float m) {
+  // m * 2^40 is exact in fp32 (an exponent shift); truncation toward zero.
+  const float scaled = m * 1099511627776.0f;
+  return scaled > 0.f ? __float2ull_rz(scaled) : 0ull;
+}
+
+__device__ __forceinline__ uint64_t warp_incl_scan(uint64_t v) {
+  const int lane = threadIdx.x % 32;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+struct SegParams {
+  int T, B, H, S_max, S_cap;
+  int budget, q_min, seg_min, seg_max;
+  double delta;
+  int K;  // number of thresholds
+  const float* mass;
+  const int32_t* pad;
+  int32_t* seg_start;
+  int32_t* seg_len;
+  int32_t* quota;
+  int32_t* n_seg;
+};
+
+// Warp-wide arg-best over segments: best = largest (key) with ties to the
+// lower index (prefer_low) or higher index; returns -1 if no lane has one.
+__device__ __forceinline__ int warp_argbest(int64_t key, int idx, bool valid,
+                                            bool want_max, bool prefer_low) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int64_t ok = __shfl_xor_sync(0xffffffffu, key, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    const bool ov = __shfl_xor_sync(0xffffffffu, valid ? 1 : 0, o) != 0;
+    bool take = false;
+    if (ov) {
+      if (!valid) {
+        take = true;
+      } else if (ok != key) {
+        take = want_max ? (ok > key) : (ok < key);
+      } else {
+        take = prefer_low ? (oi < idx) : (oi > idx);
+      }
+    }
+    if (take) {
+      key = ok;
+      idx = oi;
+      valid = true;
+    }
+  }
+  return valid ? idx : -1;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    segment_quota_kernel(SegParams p) {
+  extern __shared__ uint8_t sm[];
+  // dynamic shared layout: seg mass (u64) | rem (i64) | start | len | quota |
+  // q_floor (i32) x S_cap
+  uint64_t* s_mass = reinterpret_cast<uint64_t*>(sm);
+  int64_t* s_rem = reinterpret_cast<int64_t*>(s_mass + p.S_cap);
+  int32_t* s_start = reinterpret_cast<int32_t*>(s_rem + p.S_cap);
+  int32_t* s_len = s_start + p.S_cap;
+  int32_t* s_q = s_len + p.S_cap;
+  int32_t* s_floor = s_q + p.S_cap;
+  __shared__ int32_t s_b[kMaxK];
+  __shared__ uint64_t s_warp[kThreads / 32];
+  __shared__ uint64_t s_total;
+  __shared__ int s_nseg;
+
+  const int u = blockIdx.x;
+  const int T = p.T;
+  const int b = (u / p.H) % p.B;
+  const int pad = min(max(p.pad[b], 0), T);
+  const int n = T - pad;
+  const float* m = p.mass + static_cast<size_t>(u) * T + pad;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  int32_t* o_start = p.seg_start + static_cast<size_t>(u) * p.S_max;
+  int32_t* o_len = p.seg_len + static_cast<size_t>(u) * p.S_max;
+  int32_t* o_q = p.quota + static_cast<size_t>(u) * p.S_max;
+
+  if (n <= 0) {
+    for (int s = threadIdx.x; s < p.S_max; s += kThreads) {
+      o_start[s] = 0;
+      o_len[s] = 0;
+      o_q[s] = 0;
+    }
+    if (threadIdx.x == 0) p.n_seg[u] = 0;
+    return;
+  }
+
+  // ---- 1. prefix sums of the fixed-point mass over contiguous thread ranges
+  const int per = (n + kThreads - 1) / kThreads;
+  const int lo = min(n, threadIdx.x * per), hi = min(n, lo + per);
+  uint64_t local = 0;
+  for (int v = lo; v < hi; ++v) local += fixed_mass(m[v]);
+  const uint64_t incl = warp_incl_scan(local);
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t run = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const uint64_t t = s_warp[w];
+      s_warp[w] = run;
+      run += t;
+    }
+    s_total = run;
+  }
+  __syncthreads();
+  const uint64_t before = s_warp[warp] + incl - local;  // prefix before `lo`
+  const uint64_t S = s_total;
+
+  // ---- 2. cut points: b_k = min{t in [1,n] : C(t) >= tau_k}
+  const double S_d = __ull2double_rn(S);
+  for (int k = 1; k <= p.K; ++k) {
+    const double frac = __dmul_rn(static_cast<double>(k), p.delta);
+    const uint64_t tau = static_cast<uint64_t>(ceil(__dmul_rn(frac, S_d)));
+    if (tau == 0) {
+      if (threadIdx.x == 0) s_b[k - 1] = 1;
+    } else if (before < tau && tau <= before + local) {
+      uint64_t c = before;
+      for (int v = lo; v < hi; ++v) {
+        c += fixed_mass(m[v]);
+        if (c >= tau) {
+          s_b[k - 1] = v + 1;
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. raw segments, merge, split (serial: at most K+1 raw segments)
+  if (threadIdx.x == 0) {
+    // raw segments into s_start/s_len (drop empty)
+    int n_raw = 0, prev = 0;
+    for (int k = 0; k < p.K; ++k) {
+      const int bk = s_b[k];
+      if (bk > prev) {
+        s_start[n_raw] = prev;
+        s_len[n_raw] = bk - prev;
+        ++n_raw;
+        prev = bk;
+      }
+    }
+    if (prev < n) {
+      s_start[n_raw] = prev;
+      s_len[n_raw] = n - prev;
+      ++n_raw;
+    }
+    // merge in place
+    int n_mer = 0;
+    int cur_s = s_start[0], cur_l = s_len[0];
+    for (int r = 1; r < n_raw; ++r) {
+      if (cur_l < p.seg_min) {
+        cur_l += s_len[r];
+      } else {
+        s_start[n_mer] = cur_s;
+        s_len[n_mer] = cur_l;
+        ++n_mer;
+        cur_s = s_start[r];
+        cur_l = s_len[r];
+      }
+    }
+    if (cur_l < p.seg_min && n_mer > 0) {
+      s_len[n_mer - 1] += cur_l;
+    } else {
+      s_start[n_mer] = cur_s;
+      s_len[n_mer] = cur_l;
+      ++n_mer;
+    }
+    // split, back to front so that the merged list is read before overwritten
+    int n_out = 0;
+    for (int r = 0; r < n_mer; ++r) {
+      const int L = s_len[r];
+      n_out += (L <= p.seg_max) ? 1 : (L + p.seg_max - 1) / p.seg_max;
+    }
+    int w = n_out;
+    for (int r = n_mer - 1; r >= 0; --r) {
+      const int L = s_len[r], st = s_start[r];
+      if (L <= p.seg_max) {
+        --w;
+        s_start[w] = st;
+        s_len[w] = L;
+        continue;
+      }
+      const int c = (L + p.seg_max - 1) / p.seg_max;
+      const int base = L / c, extra = L % c;
+      // part j starts at st + j*base + min(j, extra)
+      for (int j = c - 1; j >= 0; --j) {
+        --w;
+        s_start[w] = st + j * base + min(j, extra);
+        s_len[w] = base + (j < extra ? 1 : 0);
+      }
+    }
+    s_nseg = n_out;
+  }
+  __syncthreads();
+  const int ns = s_nseg;
+
+  // ---- 4. segment masses (one warp per segment)
+  for (int s = warp; s < ns; s += kThreads / 32) {
+    uint64_t acc = 0;
+    for (int v = s_start[s] + lane; v < s_start[s] + s_len[s]; v += 32)
+      acc += fixed_mass(m[v]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) s_mass[s] = acc;
+  }
+  __syncthreads();
+
+  // ---- 5. quotas (warp 0)
+  if (warp == 0) {
+    const int budget = min(p.budget, n);
+    uint64_t Mt = 0;
+    int64_t floor_tot = 0;
+    for (int s = lane; s < ns; s += 32) {
+      s_floor[s] = min(p.q_min, s_len[s]);
+      Mt += s_mass[s];
+      floor_tot += s_floor[s];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Mt += __shfl_xor_sync(0xffffffffu, Mt, o);
+      floor_tot += __shfl_xor_sync(0xffffffffu, floor_tot, o);
+    }
+    __syncwarp();
+    if (floor_tot > budget) {
+      // heaviest segments first (ties: lower index) while budget remains
+      for (int s = lane; s < ns; s += 32) {
+        int64_t before_s = 0;
+        for (int j = 0; j < ns; ++j) {
+          const bool ahead = (s_mass[j] > s_mass[s]) || (s_mass[j] == s_mass[s] && j < s);
+          if (ahead) before_s += s_floor[j];
+        }
+        const int64_t left = budget - before_s;
+        s_q[s] = static_cast<int32_t>(left <= 0 ? 0 : (left < s_floor[s] ? left : s_floor[s]));
+      }
+      __syncwarp();
+      for (int s = lane; s < ns; s += 32) s_floor[s] = s_q[s];
+      __syncwarp();
+      floor_tot = budget;
+    }
+    const int64_t t_rem = budget - floor_tot;
+    int64_t qtot = 0;
+    for (int s = lane; s < ns; s += 32) {
+      int64_t share = 0;
+      if (Mt > 0) {
+        const uint64_t num = 2ull * static_cast<uint64_t>(t_rem) * s_mass[s] + Mt;
+        share = static_cast<int64_t>(num / (2ull * Mt));
+      }
+      int64_t q = s_floor[s] + share;
+      if (q > s_len[s]) q = s_len[s];
+      s_q[s] = static_cast<int32_t>(q);
+      s_rem[s] = (static_cast<int64_t>(s_floor[s]) * static_cast<int64_t>(Mt) +
+                  t_rem * static_cast<int64_t>(s_mass[s])) -
+                 q * static_cast<int64_t>(Mt);
+      qtot += q;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qtot += __shfl_xor_sync(0xffffffffu, qtot, o);
+    __syncwarp();
+    // correction, one unit at a time
+    while (qtot < budget) {
+      int64_t key = 0;
+      int idx = 0;
+      bool valid = false;
+      for (int s = lane; s < ns; s += 32) {
+        if (s_q[s] >= s_len[s]) continue;
+        if (!valid || s_rem[s] > key) {
+          key = s_rem[s];
+          idx = s;
+          valid = true;
+        }
+      }
+      const int best = warp_argbest(key, idx, valid, true, true);
+      if (best < 0) break;
+      if (lane == 0) {
+        s_q[best] += 1;
+        s_rem[best] -= static_cast<int64_t>(Mt);
+      }
+      __syncwarp();
+      ++qtot;
+    }
+    while (qtot > budget) {
+      int64_t key = 0;
+      int idx = 0;
+      bool valid = false;
+      for (int s = lane; s < ns; s += 32) {
+        if (s_q[s] <= s_floor[s]) continue;
+        if (!valid || s_rem[s] <= key) {  // ties -> higher index within a lane
+          key = s_rem[s];
+          idx = s;
+          valid = true;
+        }
+      }
+      const int best = warp_argbest(key, idx, valid, false, false);
+      if (best < 0) break;
+      if (lane == 0) {
+        s_q[best] -= 1;
+        s_rem[best] += static_cast<int64_t>(Mt);
+      }
+      __syncwarp();
+      --qtot;
+    }
+  }
+  __syncthreads();
+
+  // ---- 6. outputs (absolute starts), zero past n_seg
+  for (int s = threadIdx.x; s < p.S_max; s += kThreads) {
+    if (s < ns) {
+      o_start[s] = pad + s_start[s];
+      o_len[s] = s_len[s];
+      o_q[s] = s_q[s];
+    } else {
+      o_start[s] = 0;
+      o_len[s] = 0;
+      o_q[s] = 0;
+    }
+  }
+  if (threadIdx.x == 0) p.n_seg[u] = ns;
+}
+
+}  // namespace
+
+int segment_threshold_count(double delta) {
+  int K = 0;
+  for (int k = 1; k <= kMaxK + 1; ++k) {
+    if (!(static_cast<double>(k) * delta < 1.0)) break;
+    ++K;
+  }
+  return K;
+}
+
+int segment_capacity(const kvc_config& c, int T) {
+  const int K = segment_threshold_count(static_cast<double>(c.delta));
+  // raw segments (before merging) number at most K+1; after split/merge at
+  // most min(S_max, K + 1 + ceil(T/seg_max)).
+  const int bound = K + 1 + (T + c.seg_max - 1) / c.seg_max;
+  const int smax = s_max_of(c, T);
+  const int after = bound < smax ? bound : smax;
+  return after > K + 1 ? after : K + 1;
+}
+
+size_t segment_smem_bytes(const kvc_config& c, int T) {
+  return static_cast<size_t>(segment_capacity(c, T)) * (8 + 8 + 4 * 4);
+}
+
+cudaError_t launch_segment_quota(const kvc_handle* h, const float* mass, int T,
+                                 const int32_t* pad, int32_t* seg_start,
+                                 int32_t* seg_len, int32_t* quota,
+                                 int32_t* n_seg, cudaStream_t s) {
+  const kvc_config& c = h->cfg;
+  SegParams p;
+  p.T = T;
+  p.B = h->dims.B;
+  p.H = h->dims.H;
+  p.S_max = s_max_of(c, T);
+  p.S_cap = segment_capacity(c, T);
+  p.budget = c.budget;
+  p.q_min = c.q_min;
+  p.seg_min = c.seg_min;
+  p.seg_max = c.seg_max;
+  p.delta = static_cast<double>(c.delta);
+  p.K = segment_threshold_count(p.delta);
+  p.mass = mass;
+  p.pad = pad;
+  p.seg_start = seg_start;
+  p.seg_len = seg_len;
+  p.quota = quota;
+  p.n_seg = n_seg;
+  const size_t smem = segment_smem_bytes(c, T);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(segment_quota_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  segment_quota_kernel<<<h->dims.U, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvc

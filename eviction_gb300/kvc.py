@@ -1,0 +1,262 @@
+"""ctypes binding of libkvc.so (argument marshalling only).
+
+Every method maps one-to-one onto an entry point of ``include/kvc.h`` and takes
+torch tensors that must already live on the CUDA device with the documented
+dtype and layout; the binding checks dtype/device/contiguity, then passes
+``data_ptr()`` values and ``torch.cuda.current_stream()``. All arithmetic runs in
+the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, fields
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(HERE, "libkvc.so")
+
+# every function declared in include/kvc.h
+ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_sizes",
+                "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
+                "kvc_get_device_status", "kvc_last_error", "kvc_status_string")
+
+STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
+          -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
+          -8: "KVC_ERR_UNSUPPORTED"}
+
+
+class KvcError(RuntimeError):
+    def __init__(self, code, msg=""):
+        self.code = code
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+
+
+class _CConfig(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("batch", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("group", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("max_T", ctypes.c_int), ("window", ctypes.c_int),
+                ("budget", ctypes.c_int), ("avg_pool", ctypes.c_int), ("max_pool", ctypes.c_int),
+                ("delta", ctypes.c_float), ("seg_min", ctypes.c_int), ("seg_max", ctypes.c_int),
+                ("q_min", ctypes.c_int), ("n_sink", ctypes.c_int), ("n_recent", ctypes.c_int),
+                ("lambda_", ctypes.c_float), ("beta", ctypes.c_float), ("eps", ctypes.c_float),
+                ("softmax_scale", ctypes.c_float)]
+
+
+@dataclass
+class Config:
+    """Mirror of kvc_config (defaults: the method's schedule values)."""
+    n_layers: int
+    batch: int
+    n_kv_heads: int
+    group: int
+    head_dim: int
+    max_T: int
+    budget: int
+    window: int = 128
+    avg_pool: int = 5
+    max_pool: int = 7
+    delta: float = 0.1
+    seg_min: int = 16
+    seg_max: int = 256
+    q_min: int = 1
+    n_sink: int = 4
+    n_recent: int = 64
+    lam: float = 0.9
+    beta: float = 0.9
+    eps: float = 1e-6
+    softmax_scale: float = 0.0
+
+    def c(self) -> _CConfig:
+        return _CConfig(self.n_layers, self.batch, self.n_kv_heads, self.group, self.head_dim,
+                        self.max_T, self.window, self.budget, self.avg_pool, self.max_pool,
+                        self.delta, self.seg_min, self.seg_max, self.q_min, self.n_sink,
+                        self.n_recent, self.lam, self.beta, self.eps, self.softmax_scale)
+
+    @property
+    def units(self):
+        return self.n_layers * self.batch * self.n_kv_heads
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libkvc.so; raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with eviction_gb300.build.build()")
+    L = ctypes.CDLL(_LIB_PATH)
+    L.kvc_default_config.argtypes = [ctypes.POINTER(_CConfig)]
+    L.kvc_default_config.restype = None
+    L.kvc_create.argtypes = [ctypes.POINTER(_CConfig), ctypes.POINTER(_P)]
+    L.kvc_destroy.argtypes = [_P]
+    L.kvc_destroy.restype = None
+    L.kvc_stage_sizes.argtypes = [_P, _I, ctypes.POINTER(_I)]
+    L.kvc_mass.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P]
+    L.kvc_segment_quota.argtypes = [_P, _P, _I, _P, _P, _P, _P, _P, _P]
+    L.kvc_select.argtypes = [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P]
+    L.kvc_compact.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]
+    L.kvc_event.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    L.kvc_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
+    L.kvc_last_error.argtypes = [_P]
+    L.kvc_last_error.restype = ctypes.c_char_p
+    L.kvc_status_string.argtypes = [_I]
+    L.kvc_status_string.restype = ctypes.c_char_p
+    for name in ENTRY_POINTS:
+        if name not in ("kvc_default_config", "kvc_destroy", "kvc_last_error",
+                        "kvc_status_string"):
+            getattr(L, name).restype = _I
+    _lib = L
+    return L
+
+
+def _stream_ptr(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+class Handle:
+    """A kvc_handle: validated config plus the device workspace."""
+
+    def __init__(self, cfg: Config):
+        L = load_library()
+        self.cfg = cfg
+        self._c = cfg.c()
+        h = _P()
+        rc = L.kvc_create(ctypes.byref(self._c), ctypes.byref(h))
+        if rc != 0:
+            raise KvcError(rc, "kvc_create failed")
+        self._h = h
+
+    # -- helpers -------------------------------------------------------------
+    def _check(self, rc, what):
+        if rc != 0:
+            msg = load_library().kvc_last_error(self._h)
+            raise KvcError(rc, f"{what}: {msg.decode() if msg else ''}")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load_library().kvc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def s_max(self, T: int) -> int:
+        out = _I()
+        self._check(load_library().kvc_stage_sizes(self._h, T, ctypes.byref(out)), "stage_sizes")
+        return out.value
+
+    # -- entry points --------------------------------------------------------
+    def mass(self, q, k, T, pad, n_carry, credit_in, credit_post, mass, score, stream=None):
+        import torch
+        rc = load_library().kvc_mass(
+            self._h, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), T,
+            _dev(pad, torch.int32, "pad"), _dev(n_carry, torch.int32, "n_carry"),
+            _dev(credit_in, torch.float32, "credit_in"),
+            _dev(credit_post, torch.float32, "credit_post"), _dev(mass, torch.float32, "mass"),
+            _dev(score, torch.float32, "score"), _stream_ptr(stream))
+        self._check(rc, "kvc_mass")
+
+    def segment_quota(self, mass, T, pad, seg_start, seg_len, quota, n_seg, stream=None):
+        import torch
+        rc = load_library().kvc_segment_quota(
+            self._h, _dev(mass, torch.float32, "mass"), T, _dev(pad, torch.int32, "pad"),
+            _dev(seg_start, torch.int32, "seg_start"), _dev(seg_len, torch.int32, "seg_len"),
+            _dev(quota, torch.int32, "quota"), _dev(n_seg, torch.int32, "n_seg"),
+            _stream_ptr(stream))
+        self._check(rc, "kvc_segment_quota")
+
+    def select(self, score, T, pad, seg_start, seg_len, quota, n_seg, kept_idx, n_kept,
+               stream=None):
+        import torch
+        rc = load_library().kvc_select(
+            self._h, _dev(score, torch.float32, "score"), T, _dev(pad, torch.int32, "pad"),
+            _dev(seg_start, torch.int32, "seg_start"), _dev(seg_len, torch.int32, "seg_len"),
+            _dev(quota, torch.int32, "quota"), _dev(n_seg, torch.int32, "n_seg"),
+            _dev(kept_idx, torch.int32, "kept_idx"), _dev(n_kept, torch.int32, "n_kept"),
+            _stream_ptr(stream))
+        self._check(rc, "kvc_select")
+
+    def compact(self, k, v, credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out,
+                stream=None):
+        import torch
+        rc = load_library().kvc_compact(
+            self._h, _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"),
+            _dev(credit_post, torch.float32, "credit_post"), T,
+            _dev(kept_idx, torch.int32, "kept_idx"), _dev(n_kept, torch.int32, "n_kept"),
+            _dev(k_out, torch.bfloat16, "k_out"), _dev(v_out, torch.bfloat16, "v_out"),
+            _dev(credit_out, torch.float32, "credit_out"), _stream_ptr(stream))
+        self._check(rc, "kvc_compact")
+
+    def event(self, q, k, v, T, pad, n_carry, credit_in, k_out, v_out, credit_out, kept_idx,
+              n_kept, stream=None):
+        import torch
+        rc = load_library().kvc_event(
+            self._h, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"),
+            _dev(v, torch.bfloat16, "v"), T, _dev(pad, torch.int32, "pad"),
+            _dev(n_carry, torch.int32, "n_carry"), _dev(credit_in, torch.float32, "credit_in"),
+            _dev(k_out, torch.bfloat16, "k_out"), _dev(v_out, torch.bfloat16, "v_out"),
+            _dev(credit_out, torch.float32, "credit_out"),
+            _dev(kept_idx, torch.int32, "kept_idx"), _dev(n_kept, torch.int32, "n_kept"),
+            _stream_ptr(stream))
+        self._check(rc, "kvc_event")
+
+    def device_status(self, stream=None) -> int:
+        bits = ctypes.c_uint32(0)
+        rc = load_library().kvc_get_device_status(self._h, ctypes.byref(bits), _stream_ptr(stream))
+        if rc not in (0, -7):
+            self._check(rc, "kvc_get_device_status")
+        return bits.value
+
+    # -- allocation conveniences (torch allocates; the library never does) ---
+    def outputs(self, T, device="cuda"):
+        """Output tensors of one event: k_out, v_out, credit_out, kept_idx, n_kept."""
+        import torch
+        c = self.cfg
+        L, B, H, d, Kb = c.n_layers, c.batch, c.n_kv_heads, c.head_dim, c.budget
+        return dict(
+            k_out=torch.empty((L, B, H, Kb, d), dtype=torch.bfloat16, device=device),
+            v_out=torch.empty((L, B, H, Kb, d), dtype=torch.bfloat16, device=device),
+            credit_out=torch.empty((L, B, H, Kb), dtype=torch.float32, device=device),
+            kept_idx=torch.empty((L, B, H, Kb), dtype=torch.int32, device=device),
+            n_kept=torch.empty((L, B, H), dtype=torch.int32, device=device))
+
+    def stage_buffers(self, T, device="cuda"):
+        """Intermediate tensors for the stage-by-stage entry points."""
+        import torch
+        c = self.cfg
+        L, B, H = c.n_layers, c.batch, c.n_kv_heads
+        S = self.s_max(T)
+        f = dict(dtype=torch.float32, device=device)
+        i = dict(dtype=torch.int32, device=device)
+        return dict(mass=torch.empty((L, B, H, T), **f), score=torch.empty((L, B, H, T), **f),
+                    credit_post=torch.empty((L, B, H, T), **f),
+                    seg_start=torch.empty((L, B, H, S), **i),
+                    seg_len=torch.empty((L, B, H, S), **i),
+                    quota=torch.empty((L, B, H, S), **i), n_seg=torch.empty((L, B, H), **i))

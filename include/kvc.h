@@ -1,0 +1,170 @@
+/*
+ * kvc.h -- C ABI of the GB300 (sm_103a) decode-time KV-cache compression event.
+ *
+ * The event, per unit = (layer, sequence, KV head), follows
+ * "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning" (AMS),
+ * Method, Key designs 1-4:
+ *   1. attention usage of the cache by the W most recent decode queries of the
+ *      unit's GQA group (softmax of q.k/sqrt(d), summed over queries and heads;
+ *      causally unseen suffix entries filled with the window maximum);
+ *      the base score is the usage max-pooled over 7 neighbours
+ *      ("RefreshKV: Updating Small KV Cache During Long-form Generation",
+ *      A2 prefilling stage and A6 baseline settings);
+ *   2. average pool (5), clamp + eps normalisation to a mass, EMA credit mix;
+ *   3. cuts at cumulative-mass multiples of Delta, split/merge to 16..256;
+ *   4. exact-integer quotas (q_min + mass share), must-keep sinks and suffix;
+ *   5. segment-local top-k, union with must-keep, budget fix-up;
+ *   6. sort the kept slots and gather K, V and the credit into a fixed-length
+ *      cache.
+ *
+ * Memory and layout (every tensor pointer below is DEVICE memory, caller
+ * owned, C-contiguous, 16-byte aligned, with the layer dimension outermost):
+ *   q       [L][B][H*G][W][d]  bf16 (raw 16-bit patterns, uint16_t);
+ *                              query head h*G+g belongs to KV head h
+ *                              ("SkipKV: ...", A2 token importance: g(i)=floor(i/n))
+ *   k, v    [L][B][H][T][d]    bf16; slot t of a sequence with left padding
+ *                              pad[b] is valid iff t >= pad[b]
+ *   credit  [L][B][H][T]       fp32 EMA credit (Key design 1)
+ *   pad     [B]                int32 left padding per sequence, 0 <= pad <= T
+ *   n_carry [B]                int32: slots [pad, pad+n_carry) carry credit
+ *                              from the previous event; later slots are new
+ *                              and start at their current mass
+ *   mass, score               [L][B][H][T] fp32 (0 / -inf on padding)
+ *   seg_start, seg_len, quota [L][B][H][S_max] int32, S_max from
+ *                              kvc_stage_sizes; seg_start is an absolute slot
+ *   n_seg, n_kept             [L][B][H] int32
+ *   kept_idx                  [L][B][H][budget] int32 absolute slots, ascending,
+ *                              -1 past n_kept
+ *   k_out, v_out              [L][B][H][budget][d] bf16; rows past n_kept = 0
+ *   credit_out                [L][B][H][budget] fp32
+ * L, B, H, G, W, d come from the handle's config; T (<= max_T) is per call.
+ * The window's query j sits at slot T-W+j and sees slots [pad, T-W+j].
+ * n_kept = min(budget, T - pad).
+ *
+ * Calls.  Every entry point validates its arguments on the host and returns a
+ * negative KVC_ERR_* code without launching anything if they are wrong.
+ * Otherwise it enqueues its kernels on `stream` (a cudaStream_t; NULL = the
+ * legacy default stream) and returns KVC_OK without synchronising; device-side
+ * conditions are reported through kvc_get_device_status.  No entry point
+ * allocates memory except kvc_create.  A handle is not thread-safe and must
+ * not be used on two streams at once (it owns one workspace).  Outputs must
+ * not alias inputs, except credit_post may alias credit_in in kvc_mass.
+ * The caller keeps the logical (RoPE) positions of the kept tokens: the next
+ * token's position continues the original progress (AMS, Key design 4).
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------- */
+#define KVC_OK 0
+#define KVC_ERR_ARG (-1)         /* null pointer, bad config value           */
+#define KVC_ERR_SHAPE (-2)       /* T out of range for this handle           */
+#define KVC_ERR_ALIGN (-3)       /* pointer not 16-byte aligned              */
+#define KVC_ERR_NOMEM (-4)       /* workspace allocation failed (create)     */
+#define KVC_ERR_CUDA (-5)        /* a CUDA runtime call failed               */
+#define KVC_ERR_DEVICE (-6)      /* no usable sm_103 device                  */
+#define KVC_ERR_TIMEOUT (-7)     /* a bounded device wait gave up            */
+#define KVC_ERR_UNSUPPORTED (-8) /* config outside what the kernels handle   */
+
+/* ---- device status bits (kvc_get_device_status) ------------------------ */
+#define KVC_STATUS_WAIT_TIMEOUT 0x1u /* an mbarrier wait hit its bound; the
+                                        affected outputs are unspecified     */
+#define KVC_STATUS_BAD_INDEX 0x2u    /* kvc_compact got a kept index outside
+                                        [0, T): that row was written as zeros */
+
+/* ---- configuration ------------------------------------------------------ */
+typedef struct {
+  int n_layers;    /* L                                                    */
+  int batch;       /* B                                                    */
+  int n_kv_heads;  /* H                                                    */
+  int group;       /* G query heads per KV head                            */
+  int head_dim;    /* d: 64 or 128                                         */
+  int max_T;       /* largest T any call will pass, <= 65536               */
+  int window;      /* W: most recent decode queries (128); G*W <= 4096     */
+  int budget;      /* T_keep (AMS: 256/512/1024)                           */
+  int avg_pool;    /* odd, mass average pool (5)                           */
+  int max_pool;    /* odd, score max pool (7)                              */
+  float delta;     /* cumulative-mass step, delta >= 1/1024 (0.1)          */
+  int seg_min;     /* >= 1 (16)                                            */
+  int seg_max;     /* 2*seg_min <= seg_max, 16 <= seg_max <= 4096 (256)    */
+  int q_min;       /* 1                                                    */
+  int n_sink;      /* 4                                                    */
+  int n_recent;    /* recent suffix kept                                   */
+  float lambda;    /* credit EMA decay in [0,1] (0.9)                      */
+  float beta;      /* current-mass weight in [0,1] (0.9)                   */
+  float eps;       /* mass floor > 0 (1e-6)                                */
+  float softmax_scale; /* 0 => 1/sqrt(head_dim)                            */
+} kvc_config;
+
+typedef struct kvc_handle kvc_handle;
+
+/* Fill *cfg with the method's defaults (AMS schedule: W 128, Delta 0.1,
+ * lengths 16/256, q_min 1, 4 sinks, lambda = beta = 0.9; eps 1e-6; pools 5/7)
+ * and zero sizes.  The caller sets the sizes and budget. */
+void kvc_default_config(kvc_config* cfg);
+
+/* Validate `cfg`, select the current CUDA device (must be sm_103), and
+ * allocate the handle and its device workspace (sized from the config's
+ * maximum dimensions).  On success *out owns them; free with kvc_destroy. */
+int kvc_create(const kvc_config* cfg, kvc_handle** out);
+
+/* Free the handle and its workspace (synchronises the device first). */
+void kvc_destroy(kvc_handle* h);
+
+/* *s_max = max(1, T / seg_min): the segment-array stride for this T. */
+int kvc_stage_sizes(const kvc_handle* h, int T, int* s_max);
+
+/* Steps 1-2: attention usage, score, mass, credit.  Uses the handle's
+ * workspace for per-query softmax statistics and the raw usage.
+ * credit_in is read, credit_post written (they may be the same buffer). */
+int kvc_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T,
+             const int32_t* pad, const int32_t* n_carry,
+             const float* credit_in, float* credit_post, float* mass,
+             float* score, void* stream);
+
+/* Steps 3-4: segmentation and quotas on the fp32 mass.  Bit-exact integer
+ * arithmetic (40-bit fixed-point mass, exact rational comparisons). */
+int kvc_segment_quota(kvc_handle* h, const float* mass, int T,
+                      const int32_t* pad, int32_t* seg_start,
+                      int32_t* seg_len, int32_t* quota, int32_t* n_seg,
+                      void* stream);
+
+/* Step 5 (and the index sort of step 6): kept slots per unit. */
+int kvc_select(kvc_handle* h, const float* score, int T, const int32_t* pad,
+               const int32_t* seg_start, const int32_t* seg_len,
+               const int32_t* quota, const int32_t* n_seg, int32_t* kept_idx,
+               int32_t* n_kept, void* stream);
+
+/* Step 6: gather K, V and the post-EMA credit at the kept slots. */
+int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
+                const float* credit_post, int T, const int32_t* kept_idx,
+                const int32_t* n_kept, uint16_t* k_out, uint16_t* v_out,
+                float* credit_out, void* stream);
+
+/* The whole event, steps 1-6, with the intermediates in the workspace. */
+int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
+              const uint16_t* v, int T, const int32_t* pad,
+              const int32_t* n_carry, const float* credit_in,
+              uint16_t* k_out, uint16_t* v_out, float* credit_out,
+              int32_t* kept_idx, int32_t* n_kept, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status bits. */
+int kvc_get_device_status(kvc_handle* h, uint32_t* bits, void* stream);
+
+/* Human-readable text of the last error on this handle ("" if none). */
+const char* kvc_last_error(const kvc_handle* h);
+
+/* Name of a KVC_* status code. */
+const char* kvc_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H */
