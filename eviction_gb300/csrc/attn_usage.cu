@@ -14,14 +14,16 @@
 // into two tensor-core passes over the same QK^T:
 //   pass 1: rows on TMEM lanes (A = 128 query rows, B = 128-slot chunks of K);
 //           each epilogue thread owns one row and keeps an online max / sum;
-//           out: b_r = log2 of the row normaliser (in the scaled log2
-//           domain) and 1/Z'_r (the row's largest probability).
+//           out: per row (scaled log2 max, sum of exp2 relative to it).
 //   pass 2: slots on TMEM lanes (A = 128 cached keys, B = 128-row chunks of
 //           Q); each epilogue thread owns one slot and sums
-//           exp2(scale*log2e*z - b_r) over the rows.
+//           exp2(scale*log2e*z - b_r) over the rows, b_r = log2 normaliser.
 // Both passes are persistent, warp-specialised kernels: warp 0 issues TMA
 // loads into a 4-stage ring, warp 1 issues tcgen05.mma into two TMEM
-// accumulators, warps 2-5 drain the accumulators.  Every wait is bounded.
+// accumulators, and two epilogue warpgroups (warps 2-5 and 6-9) drain them:
+// warpgroup w takes every accumulator of parity w and writes partial results
+// (per-row statistics, per-slot sums) to its own half of the workspace; the
+// consumers combine the two halves.  Every wait is bounded.
 #include <cmath>
 #include <cstdio>
 
@@ -30,7 +32,8 @@
 namespace kvc {
 namespace {
 
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kEpiWarps = 8;                    // two warpgroups
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // + TMA warp + MMA warp
 constexpr int BM = 128;        // A-operand rows (TMEM lanes)
 constexpr int BN = 128;        // B-operand rows per chunk (TMEM columns)
 constexpr int kStages = 4;     // B ring depth
@@ -38,11 +41,11 @@ constexpr int kAccCols = 2 * BN;  // two accumulators
 
 struct Params {
   int U, T, R, W, B, H;
-  int n_items, n_tiles;
+  int n_items, n_tiles, r_local;  // r_local: rows of row constants per buffer
   float scale_log2;
   const int32_t* pad;
-  float2* rowstat;
-  float* usage;
+  float2* rowpart;   // [2][U][R] per-warpgroup row statistics
+  float* usage;      // [2][U][T] per-warpgroup slot sums
   uint32_t* status;
 };
 
@@ -80,14 +83,20 @@ struct Layout {
   static constexpr int kOffA = 0;
   static constexpr int kOffB = 2 * kABytes;
   static constexpr int kOffBars = kOffB + kStages * kBBytes;
-  static constexpr int kNumBars = 2 * kStages + 6 + 1 + 2;
+  static constexpr int kNumBars = 2 * kStages + 6 + 1 + 4;
   static_assert(kNumBars <= 24, "barrier area holds 24 barriers");
   static constexpr int kOffMisc = kOffBars + 24 * 8;
-  static constexpr int kOffRowB = kOffMisc + 16;   // pass 2: per-row constants x2
-  static size_t bytes(int r_pad) {
-    return 1024 + kOffRowB + 2 * static_cast<size_t>(r_pad) * 4;
+  static constexpr int kOffRowB = kOffMisc + 16;   // pass 2: row constants [2 wg][2 buf]
+  static size_t bytes(int r_local) {
+    return 1024 + kOffRowB + 4 * static_cast<size_t>(r_local) * 4;
   }
 };
+
+// Rows of row constants one warpgroup holds per item: its share of the chunks.
+__host__ __device__ inline int rows_local(int R) {
+  const int n_ch = (R + BN - 1) / BN;
+  return ((n_ch + 1) / 2) * BN;
+}
 
 // Warp-uniform wait for the epilogue warps: lane 0 waits, the result is
 // broadcast, so that the collective TMEM loads that follow run converged.
@@ -106,6 +115,33 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
   mbar_wait(bar, parity, &never, status);
 }
 
+__device__ __forceinline__ float4 lds128(const float* ptr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_u32(ptr)));
+  return v;
+}
+
+__device__ __forceinline__ float lds32(const float* ptr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(ptr)));
+  return v;
+}
+
+__device__ __forceinline__ void sts32(float* ptr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_u32(ptr)), "f"(v) : "memory");
+}
+
+// Row normaliser b_r = log2 sum_i exp2(x_i) from the two warpgroups' partial
+// (max, sum) pairs (x = scaled logits); +inf for a row that sees nothing.
+__device__ __forceinline__ float combine_row_b(float2 a, float2 b) {
+  const float m = fmaxf(a.x, b.x);
+  if (m == -INFINITY) return INFINITY;
+  const float s = a.y * ex2(a.x - m) + b.y * ex2(b.x - m);
+  return s > 0.f ? m + log2f(s) : INFINITY;
+}
+
 template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1)
     usage_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -113,8 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte alignment for the 128-byte swizzle, as an offset from the shared
+  // array so that the compiler keeps the shared address space
+  const uint32_t mis = smem_u32(smem_raw) & 1023u;
+  uint8_t* smem = smem_raw + ((1024u - mis) & 1023u);
   uint8_t* a_buf = smem + Ly::kOffA;
   uint8_t* b_buf = smem + Ly::kOffB;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kOffBars);
@@ -125,11 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* accfull = aempty + 2;         // [2]
   uint64_t* accempty = accfull + 2;       // [2] (one arrival per epilogue warp)
   uint64_t* done = accempty + 2;          // [1]
-  uint64_t* rb_full = done + 1;           // [2] per-row constants written
+  uint64_t* rb_full = done + 1;           // [2 wg][2 buf] row constants written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
   float* row_b_all = reinterpret_cast<float*>(smem + Ly::kOffRowB);
-  const int r_pad_max = ((p.R + BN - 1) / BN) * BN;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -144,8 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&accempty[b], 4);
     }
     mbar_init(done, 1);
-    mbar_init(&rb_full[0], 128);
-    mbar_init(&rb_full[1], 128);
+    for (int b = 0; b < 4; ++b) mbar_init(&rb_full[b], 128);
     *abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_a);
@@ -244,108 +280,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int wg = (warp - 2) >> 2;   // warpgroup: accumulators of parity wg
+    const int quarter = warp & 3;     // TMEM lane quarter this warp may access
     const int lrow = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t t_acc =
+        tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * BN;
     const float c = p.scale_log2;
-    int acc_iter = 0, rb_iter = 0;
+    int k_iter = 0;   // accumulators consumed by this warpgroup
+    int g = 0;        // global chunk index of the item's first chunk
+    int rb_iter = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
       const Item it = decode<PASS>(p, item);
+      const int first = (wg - g) & 1;   // first chunk of this item that is ours
+      g += it.n_ch;
       if (PASS == 1) {
         const int r = it.tile * BM + lrow;
         const int qpos = p.T - p.W + (r % p.W);
-        const bool row_valid = (r < p.R) && (qpos >= it.pad);
-        float mz = -INFINITY, sum = 0.f;
-        for (int ch = 0; ch < it.n_ch; ++ch) {
-          const int acc = acc_iter & 1;
-          if (!epi_wait(&accfull[acc], (acc_iter >> 1) & 1, abort, p.status, lane)) {
+        const bool row_valid = (r < p.R) && (qpos >= it.pad) && (it.n_ch > 0);
+        float mz = -INFINITY, sum = 0.f;  // max in raw logit units, sum rel. to it
+        for (int ch = first; ch < it.n_ch; ch += 2) {
+          if (!epi_wait(&accfull[wg], k_iter & 1, abort, p.status, lane)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const int c0 = it.c_start + ch * BN;
           const int lo = max(it.pad, c0), hi = min(qpos, c0 + BN - 1);
+          const bool fast = __all_sync(0xffffffffu,
+                                       row_valid && lo == c0 && hi == c0 + BN - 1);
 #pragma unroll 1
           for (int bt = 0; bt < BN / 32; ++bt) {
             uint32_t v[32];
             __syncwarp();
-            tmem_ld32(t_lane + acc * BN + bt * 32, v);
+            tmem_ld32(t_acc + bt * 32, v);
             tmem_ld_wait();
-            if (!row_valid) continue;
-            const int p0 = c0 + bt * 32;
-            if (p0 > hi || p0 + 31 < lo) continue;
-            const bool whole = (p0 >= lo) && (p0 + 31 <= hi);
-            float bm = -INFINITY;
-            if (whole) {
+            if (fast) {
+              float bm0 = __uint_as_float(v[0]), bm1 = __uint_as_float(v[1]);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) bm = fmaxf(bm, __uint_as_float(v[i]));
-            } else {
+              for (int i = 2; i < 32; i += 2) {
+                bm0 = fmaxf(bm0, __uint_as_float(v[i]));
+                bm1 = fmaxf(bm1, __uint_as_float(v[i + 1]));
+              }
+              const float bm = fmaxf(bm0, bm1);
+              if (bm > mz) {
+                sum *= ex2((mz - bm) * c);
+                mz = bm;
+              }
+              const float neg = -mz * c;
+              float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (p0 + i >= lo && p0 + i <= hi)
-                  bm = fmaxf(bm, __uint_as_float(v[i]));
-            }
-            if (bm > mz) {
-              sum *= ex2((mz - bm) * c);
-              mz = bm;
-            }
-            const float neg = -mz * c;
-            float s0 = 0.f, s1 = 0.f;
-            if (whole) {
-#pragma unroll
-              for (int i = 0; i < 32; i += 2) {
+              for (int i = 0; i < 32; i += 4) {
                 s0 += ex2(fmaf(__uint_as_float(v[i]), c, neg));
                 s1 += ex2(fmaf(__uint_as_float(v[i + 1]), c, neg));
+                s2 += ex2(fmaf(__uint_as_float(v[i + 2]), c, neg));
+                s3 += ex2(fmaf(__uint_as_float(v[i + 3]), c, neg));
               }
-            } else {
+              sum += (s0 + s1) + (s2 + s3);
+            } else if (row_valid) {
+              const int p0 = c0 + bt * 32;
+              float bm = -INFINITY;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (p0 + i >= lo && p0 + i <= hi) bm = fmaxf(bm, __uint_as_float(v[i]));
+              if (bm > mz) {
+                sum *= ex2((mz - bm) * c);
+                mz = bm;
+              }
+              const float neg = -mz * c;
+              float s0 = 0.f;
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (p0 + i >= lo && p0 + i <= hi)
                   s0 += ex2(fmaf(__uint_as_float(v[i]), c, neg));
+              sum += s0;
             }
-            sum += s0 + s1;
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[acc]);
-          ++acc_iter;
+          if (lane == 0) mbar_arrive(&accempty[wg]);
+          ++k_iter;
         }
         if (!ok) break;
         if (r < p.R) {
-          float2 st;
-          if (row_valid && sum > 0.f) {
-            st.x = mz * c + log2f(sum);
-            st.y = 1.0f / sum;
-          } else {
-            st.x = INFINITY;
-            st.y = 0.f;
-          }
-          p.rowstat[static_cast<size_t>(it.u) * p.R + r] = st;
+          const float2 st = (row_valid && sum > 0.f) ? make_float2(mz * c, sum)
+                                                     : make_float2(-INFINITY, 0.f);
+          p.rowpart[(static_cast<size_t>(wg) * p.U + it.u) * p.R + r] = st;
         }
       } else {
         if (it.n_ch == 0) continue;
-        // Per-row constants of this unit, padded with +inf past R, double
-        // buffered across items: every epilogue thread writes its share and
-        // arrives; a thread only rewrites a buffer after all threads arrived for
-        // the following item, i.e. after all of them finished with it.
-        const int r_pad = it.n_ch * BN;
+        // Row constants of the chunks this warpgroup takes, double buffered
+        // across items: every thread of the warpgroup writes its share and
+        // arrives; a thread only rewrites a buffer after the whole warpgroup
+        // arrived for the following item, i.e. finished with it.
         const int rb = rb_iter & 1;
-        float* row_b = row_b_all + rb * r_pad_max;
-        for (int r = lrow; r < r_pad; r += 128)
-          row_b[r] = (r < p.R) ? p.rowstat[static_cast<size_t>(it.u) * p.R + r].x
-                               : INFINITY;
-        mbar_arrive(&rb_full[rb]);
-        if (!mbar_wait(&rb_full[rb], (rb_iter >> 1) & 1, abort, p.status)) break;
+        float* row_b = row_b_all + (wg * 2 + rb) * p.r_local;
+        {
+          int l = 0;
+          for (int ch = first; ch < it.n_ch; ch += 2, ++l) {
+            const int r = ch * BN + lrow;
+            float bv = INFINITY;
+            if (r < p.R) {
+              const size_t o = static_cast<size_t>(it.u) * p.R + r;
+              bv = combine_row_b(p.rowpart[o],
+                                 p.rowpart[static_cast<size_t>(p.U) * p.R + o]);
+            }
+            sts32(row_b + l * BN + lrow, bv);
+          }
+        }
+        mbar_arrive(&rb_full[wg * 2 + rb]);
+        if (!mbar_wait(&rb_full[wg * 2 + rb], (rb_iter >> 1) & 1, abort, p.status)) break;
         ++rb_iter;
         const int pos = it.tile * BM + lrow;
         const bool pos_valid = (pos >= it.pad) && (pos < p.T);
-        const bool all_rows = pos_valid && (pos <= p.T - p.W);
+        const bool fast = __all_sync(0xffffffffu, pos_valid && (pos <= p.T - p.W));
         const int jmin = pos - (p.T - p.W);  // rows with j >= jmin see pos
-        float a0 = 0.f, a1 = 0.f;
-        for (int ch = 0; ch < it.n_ch; ++ch) {
-          const int acc = acc_iter & 1;
-          if (!epi_wait(&accfull[acc], (acc_iter >> 1) & 1, abort, p.status, lane)) {
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int l = 0;
+        for (int ch = first; ch < it.n_ch; ch += 2, ++l) {
+          if (!epi_wait(&accfull[wg], k_iter & 1, abort, p.status, lane)) {
             ok = false;
             break;
           }
@@ -354,34 +407,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int bt = 0; bt < BN / 32; ++bt) {
             uint32_t v[32];
             __syncwarp();
-            tmem_ld32(t_lane + acc * BN + bt * 32, v);
+            tmem_ld32(t_acc + bt * 32, v);
             tmem_ld_wait();
-            const int r0 = ch * BN + bt * 32;
-            if (all_rows) {
+            const float* rbb = row_b + l * BN + bt * 32;
+            if (fast) {
 #pragma unroll
               for (int i = 0; i < 32; i += 4) {
-                const float4 bb = *reinterpret_cast<const float4*>(&row_b[r0 + i]);
+                const float4 bb = lds128(rbb + i);
                 a0 += ex2(fmaf(__uint_as_float(v[i]), c, -bb.x));
                 a1 += ex2(fmaf(__uint_as_float(v[i + 1]), c, -bb.y));
-                a0 += ex2(fmaf(__uint_as_float(v[i + 2]), c, -bb.z));
-                a1 += ex2(fmaf(__uint_as_float(v[i + 3]), c, -bb.w));
+                a2 += ex2(fmaf(__uint_as_float(v[i + 2]), c, -bb.z));
+                a3 += ex2(fmaf(__uint_as_float(v[i + 3]), c, -bb.w));
               }
             } else if (pos_valid) {
+              const int r0 = ch * BN + bt * 32;
+              int j = r0 % p.W;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                const int r = r0 + i;
-                if (r < p.R && (r % p.W) >= jmin)
-                  a0 += ex2(fmaf(__uint_as_float(v[i]), c, -row_b[r]));
+                if (j >= jmin && r0 + i < p.R)
+                  a0 += ex2(fmaf(__uint_as_float(v[i]), c, -lds32(rbb + i)));
+                j = (j + 1 == p.W) ? 0 : j + 1;
               }
             }
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[acc]);
-          ++acc_iter;
+          if (lane == 0) mbar_arrive(&accempty[wg]);
+          ++k_iter;
         }
         if (!ok) break;
-        if (pos_valid) p.usage[static_cast<size_t>(it.u) * p.T + pos] = a0 + a1;
+        if (pos_valid)
+          p.usage[(static_cast<size_t>(wg) * p.U + it.u) * p.T + pos] = (a0 + a1) + (a2 + a3);
       }
     }
   }
@@ -438,7 +494,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int d,
 }
 
 template <int D>
-cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, cudaStream_t s,
+cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStream_t s,
                      std::string* err) {
   const Dims& dm = h->dims;
   CUtensorMap map_q, map_k;
@@ -455,48 +511,45 @@ cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, cudaStream_t s,
   p.H = dm.H;
   p.scale_log2 = a.scale_log2;
   p.pad = a.pad;
-  p.rowstat = h->ws.rowstat;
+  p.rowpart = h->ws.rowstat;
   p.usage = h->ws.usage;
+  p.r_local = rows_local(dm.R);
   p.status = h->ws.status;
 
-  const int r_pad = ((dm.R + BN - 1) / BN) * BN;
-  const size_t smem1 = Layout<D>::bytes(0);
-  const size_t smem2 = Layout<D>::bytes(r_pad);
   cudaError_t e;
-  e = cudaFuncSetAttribute(usage_kernel<D, 1>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem1));
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(usage_kernel<D, 2>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem2));
-  if (e != cudaSuccess) return e;
-
-  // pass 1: items = (unit, 128-row tile)
-  p.n_tiles = (dm.R + BM - 1) / BM;
-  p.n_items = dm.U * p.n_tiles;
-  int grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
-  usage_kernel<D, 1><<<grid, kThreads, smem1, s>>>(map_q, map_k, p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  // pass 2: items = (unit, 128-slot tile)
-  p.n_tiles = (a.T + BM - 1) / BM;
-  p.n_items = dm.U * p.n_tiles;
-  grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
-  usage_kernel<D, 2><<<grid, kThreads, smem2, s>>>(map_k, map_q, p);
+  if (pass == 1) {
+    // items = (unit, 128-row tile)
+    const size_t smem = Layout<D>::bytes(0);
+    e = cudaFuncSetAttribute(usage_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    p.n_tiles = (dm.R + BM - 1) / BM;
+    p.n_items = dm.U * p.n_tiles;
+    const int grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
+    usage_kernel<D, 1><<<grid, kThreads, smem, s>>>(map_q, map_k, p);
+  } else {
+    // items = (unit, 128-slot tile)
+    const size_t smem = Layout<D>::bytes(p.r_local);
+    e = cudaFuncSetAttribute(usage_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    p.n_tiles = (a.T + BM - 1) / BM;
+    p.n_items = dm.U * p.n_tiles;
+    const int grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
+    usage_kernel<D, 2><<<grid, kThreads, smem, s>>>(map_k, map_q, p);
+  }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a,
+cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a, int pass,
                                    cudaStream_t s, std::string* err) {
   switch (h->dims.d) {
     case 64:
-      return launch_d<64>(h, a, s, err);
+      return launch_d<64>(h, a, pass, s, err);
     case 128:
-      return launch_d<128>(h, a, s, err);
+      return launch_d<128>(h, a, pass, s, err);
     default:
       if (err) *err = "head_dim must be 64 or 128";
       return cudaErrorInvalidValue;
@@ -504,8 +557,8 @@ cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a,
 }
 
 size_t attention_usage_smem_bytes(int d, int R) {
-  const int r_pad = ((R + BN - 1) / BN) * BN;
-  return d == 64 ? Layout<64>::bytes(r_pad) : Layout<128>::bytes(r_pad);
+  const int rl = rows_local(R);
+  return d == 64 ? Layout<64>::bytes(rl) : Layout<128>::bytes(rl);
 }
 
 }  // namespace kvc

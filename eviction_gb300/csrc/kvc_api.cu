@@ -81,6 +81,44 @@ int cuda_fail(kvc_handle* h, cudaError_t e, const char* where) {
   return fail(h, KVC_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
 }
 
+const char* const kKernelNames[kvc::kNumKernels] = {
+    "usage_pass1_rowstats_tcgen05", "usage_pass2_colsum_tcgen05", "mass_pool_ema",
+    "segment_quota", "select_topk", "gather_compact"};
+
+cudaEvent_t prof_event(kvc_handle* h) {
+  auto& P = h->prof;
+  if (!P.pool.empty()) {
+    cudaEvent_t e = P.pool.back();
+    P.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+// Record the start of one kernel launch (nullptr when tracing is off).
+cudaEvent_t mark_begin(kvc_handle* h, cudaStream_t s) {
+  if (!h->prof.enabled) return nullptr;
+  cudaEvent_t e = prof_event(h);
+  if (e) cudaEventRecord(e, s);
+  return e;
+}
+
+void mark_end(kvc_handle* h, int kernel, cudaEvent_t begin, cudaStream_t s) {
+  if (!begin) return;
+  cudaEvent_t e = prof_event(h);
+  if (!e) {
+    h->prof.pool.push_back(begin);
+    return;
+  }
+  cudaEventRecord(e, s);
+  h->prof.pending.push_back({kernel, begin, e});
+}
+
 #define KVC_REQUIRE_PTR(p)                                                    \
   do {                                                                        \
     if (!(p)) return fail(h, KVC_ERR_ARG, "null pointer: " #p);               \
@@ -91,6 +129,59 @@ float scale_log2_of(const kvc_config& c) {
   const double s = c.softmax_scale > 0.f ? static_cast<double>(c.softmax_scale)
                                          : 1.0 / std::sqrt(static_cast<double>(c.head_dim));
   return static_cast<float>(s * 1.4426950408889634);
+}
+
+int run_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T, const int32_t* pad,
+             const int32_t* n_carry, const float* credit_in, float* credit_post, float* mass,
+             float* score, cudaStream_t s) {
+  kvc::UsageArgs a{q, k, pad, T, scale_log2_of(h->cfg)};
+  std::string err;
+  for (int pass = 1; pass <= 2; ++pass) {
+    cudaEvent_t b = mark_begin(h, s);
+    cudaError_t e = kvc::launch_attention_usage(h, a, pass, s, &err);
+    if (e != cudaSuccess)
+      return err.empty() ? cuda_fail(h, e, "attention usage") : fail(h, KVC_ERR_CUDA, err);
+    mark_end(h, pass == 1 ? kvc::kKernelUsagePass1 : kvc::kKernelUsagePass2, b, s);
+  }
+  cudaEvent_t b = mark_begin(h, s);
+  cudaError_t e =
+      kvc::launch_mass_post(h, T, pad, n_carry, credit_in, credit_post, mass, score, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "mass");
+  mark_end(h, kvc::kKernelMass, b, s);
+  return KVC_OK;
+}
+
+int run_segment_quota(kvc_handle* h, const float* mass, int T, const int32_t* pad,
+                      int32_t* seg_start, int32_t* seg_len, int32_t* quota, int32_t* n_seg,
+                      cudaStream_t s) {
+  cudaEvent_t b = mark_begin(h, s);
+  cudaError_t e =
+      kvc::launch_segment_quota(h, mass, T, pad, seg_start, seg_len, quota, n_seg, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "segment_quota");
+  mark_end(h, kvc::kKernelSegmentQuota, b, s);
+  return KVC_OK;
+}
+
+int run_select(kvc_handle* h, const float* score, int T, const int32_t* pad,
+               const int32_t* seg_start, const int32_t* seg_len, const int32_t* quota,
+               const int32_t* n_seg, int32_t* kept_idx, int32_t* n_kept, cudaStream_t s) {
+  cudaEvent_t b = mark_begin(h, s);
+  cudaError_t e = kvc::launch_select(h, score, T, pad, seg_start, seg_len, quota, n_seg,
+                                     kept_idx, n_kept, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "select");
+  mark_end(h, kvc::kKernelSelect, b, s);
+  return KVC_OK;
+}
+
+int run_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v, const float* credit_post,
+                int T, const int32_t* kept_idx, const int32_t* n_kept, uint16_t* k_out,
+                uint16_t* v_out, float* credit_out, cudaStream_t s) {
+  cudaEvent_t b = mark_begin(h, s);
+  cudaError_t e = kvc::launch_compact(h, k, v, credit_post, T, kept_idx, n_kept, k_out, v_out,
+                                      credit_out, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "compact");
+  mark_end(h, kvc::kKernelCompact, b, s);
+  return KVC_OK;
 }
 
 }  // namespace
@@ -191,8 +282,8 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
     off = align_up(off + bytes);
     return at;
   };
-  const size_t o_row = take(U * R * sizeof(float2));
-  const size_t o_use = take(U * T * 4);
+  const size_t o_row = take(2 * U * R * sizeof(float2));  // two warpgroup halves
+  const size_t o_use = take(2 * U * T * 4);
   const size_t o_mass = take(U * T * 4);
   const size_t o_score = take(U * T * 4);
   const size_t o_cp = take(U * T * 4);
@@ -237,6 +328,11 @@ void kvc_destroy(kvc_handle* h) {
     cudaDeviceSynchronize();
     cudaFree(h->ws.base);
   }
+  for (auto& m : h->prof.pending) {
+    cudaEventDestroy(m.begin);
+    cudaEventDestroy(m.end);
+  }
+  for (cudaEvent_t e : h->prof.pool) cudaEventDestroy(e);
   delete h;
 }
 
@@ -262,14 +358,8 @@ int kvc_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T,
   KVC_REQUIRE_PTR(mass);
   KVC_REQUIRE_PTR(score);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  kvc::UsageArgs a{q, k, pad, T, scale_log2_of(h->cfg)};
-  std::string err;
-  cudaError_t e = kvc::launch_attention_usage(h, a, s, &err);
-  if (e != cudaSuccess)
-    return err.empty() ? cuda_fail(h, e, "attention usage") : fail(h, KVC_ERR_CUDA, err);
-  e = kvc::launch_mass_post(h, T, pad, n_carry, credit_in, credit_post, mass, score, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "mass");
-  return KVC_OK;
+  rc = run_mass(h, q, k, T, pad, n_carry, credit_in, credit_post, mass, score, s);
+  return rc;
 }
 
 int kvc_segment_quota(kvc_handle* h, const float* mass, int T, const int32_t* pad,
@@ -284,10 +374,8 @@ int kvc_segment_quota(kvc_handle* h, const float* mass, int T, const int32_t* pa
   KVC_REQUIRE_PTR(seg_len);
   KVC_REQUIRE_PTR(quota);
   KVC_REQUIRE_PTR(n_seg);
-  cudaError_t e = kvc::launch_segment_quota(h, mass, T, pad, seg_start, seg_len, quota,
-                                            n_seg, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(h, e, "segment_quota");
-  return KVC_OK;
+  return run_segment_quota(h, mass, T, pad, seg_start, seg_len, quota, n_seg,
+                           static_cast<cudaStream_t>(stream));
 }
 
 int kvc_select(kvc_handle* h, const float* score, int T, const int32_t* pad,
@@ -304,10 +392,8 @@ int kvc_select(kvc_handle* h, const float* score, int T, const int32_t* pad,
   KVC_REQUIRE_PTR(n_seg);
   KVC_REQUIRE_PTR(kept_idx);
   KVC_REQUIRE_PTR(n_kept);
-  cudaError_t e = kvc::launch_select(h, score, T, pad, seg_start, seg_len, quota, n_seg,
-                                     kept_idx, n_kept, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(h, e, "select");
-  return KVC_OK;
+  return run_select(h, score, T, pad, seg_start, seg_len, quota, n_seg, kept_idx, n_kept,
+                    static_cast<cudaStream_t>(stream));
 }
 
 int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
@@ -325,10 +411,8 @@ int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
   KVC_REQUIRE_PTR(k_out);
   KVC_REQUIRE_PTR(v_out);
   KVC_REQUIRE_PTR(credit_out);
-  cudaError_t e = kvc::launch_compact(h, k, v, credit_post, T, kept_idx, n_kept, k_out,
-                                      v_out, credit_out, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(h, e, "compact");
-  return KVC_OK;
+  return run_compact(h, k, v, credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out,
+                     static_cast<cudaStream_t>(stream));
 }
 
 int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -351,21 +435,66 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_
   KVC_REQUIRE_PTR(n_kept);
   const kvc::Workspace& w = h->ws;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  kvc::UsageArgs a{q, k, pad, T, scale_log2_of(h->cfg)};
-  std::string err;
-  cudaError_t e = kvc::launch_attention_usage(h, a, s, &err);
-  if (e != cudaSuccess)
-    return err.empty() ? cuda_fail(h, e, "attention usage") : fail(h, KVC_ERR_CUDA, err);
-  e = kvc::launch_mass_post(h, T, pad, n_carry, credit_in, w.credit_post, w.mass, w.score, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "mass");
-  e = kvc::launch_segment_quota(h, w.mass, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "segment_quota");
-  e = kvc::launch_select(h, w.score, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg,
-                         kept_idx, n_kept, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "select");
-  e = kvc::launch_compact(h, k, v, w.credit_post, T, kept_idx, n_kept, k_out, v_out,
-                          credit_out, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "compact");
+  rc = run_mass(h, q, k, T, pad, n_carry, credit_in, w.credit_post, w.mass, w.score, s);
+  if (rc) return rc;
+  rc = run_segment_quota(h, w.mass, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, s);
+  if (rc) return rc;
+  rc = run_select(h, w.score, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, kept_idx,
+                  n_kept, s);
+  if (rc) return rc;
+  return run_compact(h, k, v, w.credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out, s);
+}
+
+int kvc_profile(kvc_handle* h, int enable) {
+  if (!h) return KVC_ERR_ARG;
+  auto& P = h->prof;
+  if (enable) {
+    for (auto& m : P.pending) {
+      cudaEventSynchronize(m.end);
+      P.pool.push_back(m.begin);
+      P.pool.push_back(m.end);
+    }
+    P.pending.clear();
+    for (int i = 0; i < kvc::kNumKernels; ++i) {
+      P.launches[i] = 0;
+      P.total_ms[i] = 0.0;
+    }
+  }
+  P.enabled = enable != 0;
+  return KVC_OK;
+}
+
+int kvc_profile_read(kvc_handle* h, kvc_kernel_time* out, int capacity, int* n_out,
+                     int reset) {
+  if (!h || (!out && capacity > 0) || !n_out) return KVC_ERR_ARG;
+  auto& P = h->prof;
+  for (auto& m : P.pending) {
+    cudaError_t e = cudaEventSynchronize(m.end);
+    float ms = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, m.begin, m.end);
+    if (e != cudaSuccess) return cuda_fail(h, e, "profile read");
+    P.launches[m.kernel] += 1;
+    P.total_ms[m.kernel] += ms;
+    P.pool.push_back(m.begin);
+    P.pool.push_back(m.end);
+  }
+  P.pending.clear();
+  int n = 0;
+  for (int i = 0; i < kvc::kNumKernels; ++i) {
+    if (n < capacity) {
+      out[n].name = kKernelNames[i];
+      out[n].launches = P.launches[i];
+      out[n].total_ms = P.total_ms[i];
+    }
+    ++n;
+  }
+  *n_out = n < capacity ? n : capacity;
+  if (reset) {
+    for (int i = 0; i < kvc::kNumKernels; ++i) {
+      P.launches[i] = 0;
+      P.total_ms[i] = 0.0;
+    }
+  }
   return KVC_OK;
 }
 

@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <vector>
 
 #include "kvc.h"
 
@@ -17,8 +18,8 @@ namespace kvc {
 // ---------------------------------------------------------------- handle ----
 
 struct Workspace {
-  float2* rowstat = nullptr;    // [U][R]  {log2 normaliser b_r, 1/Z'_r}
-  float* usage = nullptr;       // [U][max_T] raw usage (no fill)
+  float2* rowstat = nullptr;    // [2][U][R] partial row stats {scaled max, sum}
+  float* usage = nullptr;       // [2][U][max_T] partial raw usage (no fill)
   float* mass = nullptr;        // [U][max_T]   (event intermediates)
   float* score = nullptr;       // [U][max_T]
   float* credit_post = nullptr; // [U][max_T]
@@ -37,6 +38,34 @@ struct Dims {
 
 }  // namespace kvc
 
+namespace kvc {
+
+enum KernelId {
+  kKernelUsagePass1 = 0,
+  kKernelUsagePass2,
+  kKernelMass,
+  kKernelSegmentQuota,
+  kKernelSelect,
+  kKernelCompact,
+  kNumKernels
+};
+
+// Per-kernel CUDA-event tracing (see kvc_profile in kvc.h).
+struct Profiler {
+  bool enabled = false;
+  struct Mark {
+    int kernel;
+    cudaEvent_t begin, end;
+  };
+  std::vector<cudaEvent_t> pool;
+  std::vector<Mark> pending;
+  cudaEvent_t last = nullptr;  // most recent event on the traced stream
+  int launches[kNumKernels] = {};
+  double total_ms[kNumKernels] = {};
+};
+
+}  // namespace kvc
+
 struct kvc_handle {
   kvc_config cfg;
   kvc::Dims dims;
@@ -44,6 +73,7 @@ struct kvc_handle {
   int device = 0;
   int num_sms = 0;
   std::string last_error;
+  kvc::Profiler prof;
 };
 
 namespace kvc {
@@ -59,9 +89,9 @@ struct UsageArgs {
   float scale_log2;  // softmax scale * log2(e)
 };
 
-// Pass 1 + pass 2 of the window attention usage (tcgen05 kernels).
+// One pass (1 or 2) of the window attention usage (tcgen05 kernels).
 cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a,
-                                   cudaStream_t s, std::string* err);
+                                   int pass, cudaStream_t s, std::string* err);
 
 cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
                              const int32_t* n_carry, const float* credit_in,

@@ -60,32 +60,84 @@ struct SegParams {
   int32_t* n_seg;
 };
 
-// Warp-wide arg-best over segments: best = largest (key) with ties to the
-// lower index (prefer_low) or higher index; returns -1 if no lane has one.
-__device__ __forceinline__ int warp_argbest(int64_t key, int idx, bool valid,
-                                            bool want_max, bool prefer_low) {
+// The correction steps of the quota rule, in bulk.  Each step gives (or takes)
+// one unit to the segment with the best current remainder, and a segment's
+// remainder moves by the mass total Mt per unit, so the steps taken are exactly
+// the D best "bids" b_s(k) = rem_s -/+ k*Mt over k < cap_s, ordered by value and
+// then by segment index.  A search for the D-th bid value followed by an ordered
+// pass over the ties reproduces the sequential result.
+//   short (negate = false): bids rem_s - k*Mt, cap_s = len_s - q_s; q_s += taken
+//   over  (negate = true):  bids -rem_s - k*Mt, cap_s = q_s - floor_s; q_s -= taken
+__device__ __forceinline__ int64_t bids_ge(int64_t b0, int64_t M, int64_t cap, int64_t v) {
+  if (cap <= 0 || b0 < v) return 0;
+  const int64_t k = (b0 - v) / M + 1;
+  return k < cap ? k : cap;
+}
+
+__device__ void take_best_bids(const int64_t* rem, const int32_t* ref, int32_t* q, int ns,
+                               int64_t M, int64_t D,
+                               bool negate, bool low_first, int lane) {
+  auto b0_of = [&](int s) { return negate ? -rem[s] : rem[s]; };
+  auto cap_of = [&](int s) -> int64_t {
+    return negate ? static_cast<int64_t>(q[s]) - ref[s] : static_cast<int64_t>(ref[s]) - q[s];
+  };
+  // search range: every bid lies in [lo, hi]
+  int64_t lo = INT64_MAX, hi = INT64_MIN;
+  for (int s = lane; s < ns; s += 32) {
+    const int64_t cap = cap_of(s);
+    if (cap <= 0) continue;
+    const int64_t b0 = b0_of(s);
+    hi = b0 > hi ? b0 : hi;
+    const int64_t last = b0 - (cap - 1) * M;
+    lo = last < lo ? last : lo;
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const int64_t ok = __shfl_xor_sync(0xffffffffu, key, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    const bool ov = __shfl_xor_sync(0xffffffffu, valid ? 1 : 0, o) != 0;
-    bool take = false;
-    if (ov) {
-      if (!valid) {
-        take = true;
-      } else if (ok != key) {
-        take = want_max ? (ok > key) : (ok < key);
-      } else {
-        take = prefer_low ? (oi < idx) : (oi > idx);
-      }
-    }
-    if (take) {
-      key = ok;
-      idx = oi;
-      valid = true;
-    }
+    const int64_t ol = __shfl_xor_sync(0xffffffffu, lo, o);
+    const int64_t oh = __shfl_xor_sync(0xffffffffu, hi, o);
+    lo = ol < lo ? ol : lo;
+    hi = oh > hi ? oh : hi;
   }
-  return valid ? idx : -1;
+  if (lo > hi) return;  // no bids (cannot happen for a consistent input)
+  auto count_ge = [&](int64_t v) {
+    int64_t c = 0;
+    for (int s = lane; s < ns; s += 32) c += bids_ge(b0_of(s), M, cap_of(s), v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    return c;
+  };
+  // v* = largest v with count_ge(v) >= D
+  if (count_ge(lo) < D) D = count_ge(lo);  // cannot happen: total bids >= D
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo + 1) / 2;
+    if (count_ge(mid) >= D) lo = mid; else hi = mid - 1;
+  }
+  const int64_t vstar = lo;
+  // bids strictly above v*, then the ties at v* in index order
+  int64_t above = 0;
+  for (int s = lane; s < ns; s += 32) above += bids_ge(b0_of(s), M, cap_of(s), vstar + 1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+  int64_t ties_left = D - above;
+  const int n_chunks = (ns + 31) / 32;
+  for (int cc = 0; cc < n_chunks; ++cc) {
+    const int chunk = low_first ? cc : n_chunks - 1 - cc;
+    const int s = chunk * 32 + lane;
+    int64_t t = 0;
+    bool tie = false;
+    if (s < ns) {
+      const int64_t b0 = b0_of(s), cap = cap_of(s);
+      t = bids_ge(b0, M, cap, vstar + 1);
+      tie = bids_ge(b0, M, cap, vstar) > t;
+    }
+    const uint32_t ball = __ballot_sync(0xffffffffu, tie);
+    const uint32_t before = low_first ? (ball & ((1u << lane) - 1u))
+                                      : (lane == 31 ? 0u : (ball & ~((2u << lane) - 1u)));
+    if (tie && static_cast<int64_t>(__popc(before)) < ties_left) t += 1;
+    ties_left -= __popc(ball);
+    if (s < ns) q[s] = static_cast<int32_t>(negate ? q[s] - t : q[s] + t);
+    __syncwarp();
+  }
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -297,48 +349,17 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) qtot += __shfl_xor_sync(0xffffffffu, qtot, o);
     __syncwarp();
-    // correction, one unit at a time
-    while (qtot < budget) {
-      int64_t key = 0;
-      int idx = 0;
-      bool valid = false;
-      for (int s = lane; s < ns; s += 32) {
-        if (s_q[s] >= s_len[s]) continue;
-        if (!valid || s_rem[s] > key) {
-          key = s_rem[s];
-          idx = s;
-          valid = true;
-        }
-      }
-      const int best = warp_argbest(key, idx, valid, true, true);
-      if (best < 0) break;
-      if (lane == 0) {
-        s_q[best] += 1;
-        s_rem[best] -= static_cast<int64_t>(Mt);
-      }
-      __syncwarp();
-      ++qtot;
-    }
-    while (qtot > budget) {
-      int64_t key = 0;
-      int idx = 0;
-      bool valid = false;
-      for (int s = lane; s < ns; s += 32) {
-        if (s_q[s] <= s_floor[s]) continue;
-        if (!valid || s_rem[s] <= key) {  // ties -> higher index within a lane
-          key = s_rem[s];
-          idx = s;
-          valid = true;
-        }
-      }
-      const int best = warp_argbest(key, idx, valid, false, false);
-      if (best < 0) break;
-      if (lane == 0) {
-        s_q[best] -= 1;
-        s_rem[best] += static_cast<int64_t>(Mt);
-      }
-      __syncwarp();
-      --qtot;
+    // correction to the exact budget (bulk form of the one-unit-at-a-time rule)
+    if (qtot < budget) {
+      // segment s bids rem_s - k*Mt for k < L_s - q_s; take the D largest,
+      // ties between segments -> lower index first.
+      take_best_bids(s_rem, s_len, s_q, ns, static_cast<int64_t>(Mt),
+                     budget - qtot, /*negate=*/false, /*low_first=*/true, lane);
+    } else if (qtot > budget) {
+      // segment s bids rem_s + k*Mt for k < q_s - floor_s; take the D smallest,
+      // ties -> higher index first (the negated bids, largest first).
+      take_best_bids(s_rem, s_floor, s_q, ns, static_cast<int64_t>(Mt),
+                     qtot - budget, /*negate=*/true, /*low_first=*/false, lane);
     }
   }
   __syncthreads();

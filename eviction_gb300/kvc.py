@@ -18,7 +18,8 @@ _LIB_PATH = os.path.join(HERE, "libkvc.so")
 # every function declared in include/kvc.h
 ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_sizes",
                 "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
-                "kvc_get_device_status", "kvc_last_error", "kvc_status_string")
+                "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
+                "kvc_profile_read")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -29,6 +30,11 @@ class KvcError(RuntimeError):
     def __init__(self, code, msg=""):
         self.code = code
         super().__init__(f"{STATUS.get(code, code)}: {msg}")
+
+
+class _KernelTime(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int),
+                ("total_ms", ctypes.c_double)]
 
 
 class _CConfig(ctypes.Structure):
@@ -108,6 +114,8 @@ def load_library():
     L.kvc_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
     L.kvc_last_error.argtypes = [_P]
     L.kvc_last_error.restype = ctypes.c_char_p
+    L.kvc_profile.argtypes = [_P, _I]
+    L.kvc_profile_read.argtypes = [_P, ctypes.POINTER(_KernelTime), _I, ctypes.POINTER(_I), _I]
     L.kvc_status_string.argtypes = [_I]
     L.kvc_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -233,6 +241,45 @@ class Handle:
         if rc not in (0, -7):
             self._check(rc, "kvc_get_device_status")
         return bits.value
+
+    # -- tracing ---------------------------------------------------------------
+    def profile(self, enable: bool = True):
+        """Start (clearing totals) or stop per-kernel CUDA-event tracing."""
+        self._check(load_library().kvc_profile(self._h, 1 if enable else 0), "kvc_profile")
+
+    def profile_read(self, reset: bool = False):
+        """[{name, launches, total_ms}] per kernel (waits for the recorded events)."""
+        arr = (_KernelTime * 16)()
+        n = _I()
+        self._check(load_library().kvc_profile_read(self._h, arr, 16, ctypes.byref(n),
+                                                    1 if reset else 0), "kvc_profile_read")
+        return [dict(name=arr[i].name.decode(), launches=arr[i].launches,
+                     total_ms=arr[i].total_ms) for i in range(n.value)]
+
+    # -- end to end from host buffers ------------------------------------------
+    def event_host(self, host_in: dict, dev_in: dict, host_out: dict, dev_out: dict, T: int,
+                   stream=None):
+        """One event from pinned host inputs to pinned host outputs.
+
+        Copies q, k, v, credit, pad, n_carry host -> device into `dev_in`, runs
+        kvc_event into `dev_out`, copies every output back into `host_out`, all
+        on one stream (asynchronous; the caller synchronises). Returns the bytes
+        moved each way.
+        """
+        import torch
+        s = stream if stream is not None else torch.cuda.current_stream()
+        h2d = d2h = 0
+        with torch.cuda.stream(s):
+            for key in ("q", "k", "v", "credit", "pad", "n_carry"):
+                dev_in[key].copy_(host_in[key], non_blocking=True)
+                h2d += host_in[key].numel() * host_in[key].element_size()
+            self.event(dev_in["q"], dev_in["k"], dev_in["v"], T, dev_in["pad"],
+                       dev_in["n_carry"], dev_in["credit"], dev_out["k_out"], dev_out["v_out"],
+                       dev_out["credit_out"], dev_out["kept_idx"], dev_out["n_kept"], stream=s)
+            for key in ("k_out", "v_out", "credit_out", "kept_idx", "n_kept"):
+                host_out[key].copy_(dev_out[key], non_blocking=True)
+                d2h += dev_out[key].numel() * dev_out[key].element_size()
+        return h2d, d2h
 
     # -- allocation conveniences (torch allocates; the library never does) ---
     def outputs(self, T, device="cuda"):

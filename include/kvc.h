@@ -155,6 +155,27 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
               uint16_t* k_out, uint16_t* v_out, float* credit_out,
               int32_t* kept_idx, int32_t* n_kept, void* stream);
 
+/* ---- tracing -------------------------------------------------------------
+ * While enabled, every entry point records a CUDA event on its stream after
+ * each kernel it launches (and one before the first), so that the time of each
+ * kernel launch is known without a profiler.  Recording costs about a
+ * microsecond per kernel and never synchronises.  kvc_profile_read waits for
+ * the recorded events, then reports per kernel its launch count and summed
+ * duration (ms, event to event on the launch stream). */
+typedef struct {
+  const char* name;   /* static string owned by the library */
+  int launches;
+  double total_ms;
+} kvc_kernel_time;
+
+/* enable != 0 starts recording (clearing earlier totals); 0 stops. */
+int kvc_profile(kvc_handle* h, int enable);
+
+/* Copy up to `capacity` per-kernel totals into out[], the count into *n_out;
+ * reset != 0 clears the totals afterwards. */
+int kvc_profile_read(kvc_handle* h, kvc_kernel_time* out, int capacity,
+                     int* n_out, int reset);
+
 /* Synchronise `stream`, then read and clear the device status bits. */
 int kvc_get_device_status(kvc_handle* h, uint32_t* bits, void* stream);
 
