@@ -13,33 +13,35 @@
 //   * B = min(T_keep, n); n_s = min(n_sink, B); n_r = min(n_recent, B - n_s);
 //   * segment i picks max(0, q_i - |MK in i|) of its non-must-keep slots;
 //   * order: score descending, ties -> lower slot; removal of the excess picks
-//     in the exact reverse order.
-// Keys are 64-bit: (order-preserving score bits << 32) | ~slot, so "best
-// first" is descending key and every key is unique.  In-segment ranks are
-// counted directly (segments are at most seg_max long); the global excess is
-// removed with a bitwise search for the excess-th smallest pick key.
+//     in the exact reverse order (score ascending, ties -> higher slot).
+// Scores are compared through an order-preserving 32-bit key.  Each warp takes
+// whole segments: a bitwise search finds the want-th largest key among the
+// segment's candidates, then one ordered ballot pass takes the ties at that key
+// lowest slot first.  The global excess is removed the same way across the CTA
+// (bitwise search for the excess-th smallest pick key, ties highest slot first).
 #include "kvc_internal.cuh"
 
 namespace kvc {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 
-__device__ __forceinline__ uint64_t sel_key(float score, int v) {
-  return (static_cast<uint64_t>(float_order_key(score)) << 32) |
-         static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(v));
+enum : uint8_t { kOut = 0, kMust = 1, kPick = 2 };
+
+__device__ __forceinline__ uint32_t score_key(const float* sc, int v) {
+  return float_order_key(__ldg(sc + v));
 }
 
 __device__ __forceinline__ int block_count(int v, int* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  v = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(v)));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __syncthreads();
   if (lane == 0) red[warp] = v;
   __syncthreads();
   int t = 0;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) t += red[w];
+  for (int w = 0; w < kWarps; ++w) t += red[w];
   return t;
 }
 
@@ -55,15 +57,45 @@ struct SelParams {
   int32_t* n_kept;
 };
 
-// flags: 0 = out, 1 = must-keep, 2 = pick
+// One warp: mark the `want` best candidates (flag == kOut) of [st, en).
+__device__ __forceinline__ void pick_segment(const float* sc, uint8_t* flag, int st, int en,
+                                             int want, int lane) {
+  // largest x with #(candidates with key >= x) >= want: the want-th largest key
+  uint32_t x = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t t = x | (1u << bit);
+    unsigned cnt = 0;
+    for (int v = st + lane; v < en; v += 32)
+      cnt += (flag[v] == kOut && score_key(sc, v) >= t) ? 1u : 0u;
+    if (static_cast<int>(__reduce_add_sync(0xffffffffu, cnt)) >= want) x = t;
+  }
+  unsigned gt = 0;
+  for (int v = st + lane; v < en; v += 32)
+    gt += (flag[v] == kOut && score_key(sc, v) > x) ? 1u : 0u;
+  int ties_left = want - static_cast<int>(__reduce_add_sync(0xffffffffu, gt));
+  const uint32_t below = (1u << lane) - 1u;
+  for (int base = st; base < en; base += 32) {
+    const int v = base + lane;
+    const bool cand = v < en && flag[v] == kOut;
+    const uint32_t k = cand ? score_key(sc, v) : 0u;
+    const bool tie = cand && k == x;
+    const uint32_t ball = __ballot_sync(0xffffffffu, tie);
+    const bool take = (cand && k > x) ||
+                      (tie && static_cast<int>(__popc(ball & below)) < ties_left);
+    ties_left -= __popc(ball);
+    __syncwarp();
+    if (take) flag[v] = kPick;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads)
     select_kernel(SelParams p) {
   extern __shared__ uint8_t sm[];
-  int32_t* s_start = reinterpret_cast<int32_t*>(sm);        // [S_max] valid offset
-  int32_t* s_want = s_start + p.S_max;                       // [S_max]
+  int32_t* s_start = reinterpret_cast<int32_t*>(sm);             // [S_max] valid offset
+  int32_t* s_want = s_start + p.S_max;                            // [S_max]
   uint8_t* flag = reinterpret_cast<uint8_t*>(s_want + p.S_max);  // [T]
-  __shared__ int red[kThreads / 32];
-  __shared__ int s_scan[kThreads / 32];
+  __shared__ int red[kWarps];
+  __shared__ int s_scan[kWarps];
 
   const int u = blockIdx.x;
   const int T = p.T;
@@ -73,92 +105,102 @@ __global__ void __launch_bounds__(kThreads)
   const float* sc = p.score + static_cast<size_t>(u) * T + pad;
   int32_t* out = p.kept_idx + static_cast<size_t>(u) * p.budget;
   const int ns = (n > 0) ? min(max(p.n_seg[u], 0), p.S_max) : 0;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   const int Bk = min(p.budget, max(n, 0));
   const int n_s = min(p.n_sink, Bk);
   const int n_r = min(p.n_recent, Bk - n_s);
 
   // segment starts (valid offsets) and picks wanted per segment
+  int want_sum = 0;
   for (int s = threadIdx.x; s < ns; s += kThreads) {
     const int st = min(max(p.seg_start[static_cast<size_t>(u) * p.S_max + s] - pad, 0), n);
     const int L = p.seg_len[static_cast<size_t>(u) * p.S_max + s];
     const int q = p.quota[static_cast<size_t>(u) * p.S_max + s];
-    const int mk = max(0, min(st + L, n_s) - st) +
-                   max(0, st + L - max(st, n - n_r));
+    const int mk = max(0, min(st + L, n_s) - st) + max(0, st + L - max(st, n - n_r));
+    const int want = max(0, min(q - mk, L - mk));
     s_start[s] = st;
-    s_want[s] = min(max(0, q - mk), L - mk);
+    s_want[s] = want;
+    want_sum += want;
+  }
+  for (int v = threadIdx.x; v < n; v += kThreads)
+    flag[v] = (v < n_s || v >= n - n_r) ? kMust : kOut;
+  const int total_picks = block_count(want_sum, red);  // (also orders the writes above)
+
+  // segment-local picks, one warp per segment
+  for (int s = warp; s < ns; s += kWarps) {
+    const int st = s_start[s];
+    const int en = (s + 1 < ns) ? max(st, s_start[s + 1]) : n;
+    const int want = s_want[s];
+    if (want > 0) pick_segment(sc, flag, st, en, want, lane);
   }
   __syncthreads();
 
-  // ranks inside segments
-  int picks = 0;
-  for (int v = threadIdx.x; v < n; v += kThreads) {
-    const bool must = (v < n_s) || (v >= n - n_r);
-    uint8_t f = must ? 1 : 0;
-    if (!must && ns > 0) {
-      int lo = 0, hi = ns - 1;  // last segment with start <= v
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) / 2;
-        if (s_start[mid] <= v) lo = mid; else hi = mid - 1;
-      }
-      const int st = s_start[lo];
-      const int en = (lo + 1 < ns) ? max(st, s_start[lo + 1]) : n;
-      const int want = s_want[lo];
-      if (want > 0) {
-        const uint64_t key = sel_key(sc[v], v);
-        int rank = 0;
-        for (int w = st; w < en && rank < want; ++w) {
-          if (w < n_s || w >= n - n_r) continue;
-          rank += (sel_key(sc[w], w) > key) ? 1 : 0;
-        }
-        if (rank < want) {
-          f = 2;
-          ++picks;
-        }
-      }
-    }
-    flag[v] = f;
-  }
-  const int total_picks = block_count(picks, red);
+  // over budget: drop the `excess` worst picks (score ascending, ties: higher slot)
   const int excess = n_s + n_r + total_picks - Bk;
-
+  const int per = (n + kThreads - 1) / kThreads;
+  const int lo = min(n, static_cast<int>(threadIdx.x) * per);
+  const int hi = min(n, lo + per);
   if (excess > 0) {
-    // the excess-th smallest pick key: largest x with #{picks with key < x} < excess
-    uint64_t x = 0;
-    for (int bit = 63; bit >= 0; --bit) {
-      const uint64_t trial = x | (1ull << bit);
+    // x = the excess-th smallest pick key: largest x with #(pick key < x) < excess
+    uint32_t x = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t t = x | (1u << bit);
       int cnt = 0;
-      for (int v = threadIdx.x; v < n; v += kThreads)
-        if (flag[v] == 2 && sel_key(sc[v], v) < trial) ++cnt;
-      if (block_count(cnt, red) < excess) x = trial;
+      for (int v = lo; v < hi; ++v) cnt += (flag[v] == kPick && score_key(sc, v) < t) ? 1 : 0;
+      if (block_count(cnt, red) < excess) x = t;
     }
-    for (int v = threadIdx.x; v < n; v += kThreads)
-      if (flag[v] == 2 && sel_key(sc[v], v) <= x) flag[v] = 0;
+    int lt = 0, ties = 0;
+    for (int v = lo; v < hi; ++v) {
+      if (flag[v] != kPick) continue;
+      const uint32_t k = score_key(sc, v);
+      lt += (k < x) ? 1 : 0;
+      ties += (k == x) ? 1 : 0;
+    }
+    const int drop_ties = excess - block_count(lt, red);
+    // ties above this thread's range (higher slots are dropped first)
+    int incl = ties;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_down_sync(0xffffffffu, incl, o);
+      if (lane + o < 32) incl += t;
+    }
+    if (lane == 0) s_scan[warp] = incl;
+    __syncthreads();
+    int after = incl - ties;  // ties in higher lanes of this warp
+    for (int w = warp + 1; w < kWarps; ++w) after += s_scan[w];
+    for (int v = hi - 1; v >= lo; --v) {
+      if (flag[v] != kPick) continue;
+      const uint32_t k = score_key(sc, v);
+      if (k < x) {
+        flag[v] = kOut;
+      } else if (k == x) {
+        if (after < drop_ties) flag[v] = kOut;
+        ++after;
+      }
+    }
     __syncthreads();
   }
 
   // ordered write-out: contiguous ranges per thread + block exclusive scan
-  const int per = (n + kThreads - 1) / kThreads;
-  const int lo = min(n, static_cast<int>(threadIdx.x) * per);
-  const int hi = min(n, lo + per);
   int cnt = 0;
-  for (int v = lo; v < hi; ++v) cnt += flag[v] ? 1 : 0;
+  for (int v = lo; v < hi; ++v) cnt += flag[v] != kOut ? 1 : 0;
   int incl = cnt;
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int t = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += t;
   }
+  __syncthreads();  // s_scan may still be read by the excess pass
   if (lane == 31) s_scan[warp] = incl;
   __syncthreads();
   int wbase = 0;
   for (int w = 0; w < warp; ++w) wbase += s_scan[w];
   int pos = wbase + incl - cnt;
   for (int v = lo; v < hi; ++v)
-    if (flag[v] && pos < p.budget) out[pos++] = pad + v;
+    if (flag[v] != kOut && pos < p.budget) out[pos++] = pad + v;
   int total = 0;
-  for (int w = 0; w < kThreads / 32; ++w) total += s_scan[w];
+  for (int w = 0; w < kWarps; ++w) total += s_scan[w];
   for (int r = total + threadIdx.x; r < p.budget; r += kThreads) out[r] = -1;
   if (threadIdx.x == 0) p.n_kept[u] = min(total, p.budget);
 }
