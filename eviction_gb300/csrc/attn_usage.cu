@@ -12,18 +12,22 @@
 // Each softmax row needs its normaliser before its probabilities can be summed
 // per slot, and the normaliser spans every slot.  The work is therefore split
 // into two tensor-core passes over the same QK^T:
-//   pass 1: rows on TMEM lanes (A = 128 query rows, B = 128-slot chunks of K);
+//   pass 1: rows on TMEM lanes (A = query rows, B = 128-slot chunks of K);
 //           each epilogue thread owns one row and keeps an online max / sum;
-//           out: per row (scaled log2 max, sum of exp2 relative to it).
-//   pass 2: slots on TMEM lanes (A = 128 cached keys, B = 128-row chunks of
-//           Q); each epilogue thread owns one slot and sums
-//           exp2(scale*log2e*z - b_r) over the rows, b_r = log2 normaliser.
-// Both passes are persistent, warp-specialised kernels: warp 0 issues TMA
-// loads into a 4-stage ring, warp 1 issues tcgen05.mma into two TMEM
-// accumulators, and two epilogue warpgroups (warps 2-5 and 6-9) drain them:
-// warpgroup w takes every accumulator of parity w and writes partial results
-// (per-row statistics, per-slot sums) to its own half of the workspace; the
-// consumers combine the two halves.  Every wait is bounded.
+//           out: -b_r (b_r = log2 of the row normaliser in the scaled log2
+//           domain) and 1/Z'_r (the row's largest probability).
+//   pass 2: slots on TMEM lanes (A = cached keys, B = 128-row chunks of Q);
+//           each epilogue thread owns one slot and sums
+//           exp2(scale*log2e*z - b_r) over the rows.
+// Work item = one unit and a PAIR of 128-row A tiles: every B chunk that TMA
+// brings in feeds two MMAs (one per tile), which halves the operand traffic
+// per FLOP.  Persistent warp-specialised CTAs: warp 0 issues TMA loads (A
+// double-buffered across items, B through a ring), warp 1 issues tcgen05.mma
+// into four TMEM accumulators (tile x parity), warpgroup 0 (warps 2-5) drains
+// tile 0 and warpgroup 1 (warps 6-9) tile 1; each epilogue thread copies a
+// whole accumulator row to registers, hands the accumulator back, then
+// computes.  In pass 2 the row constants of the item's unit arrive by a bulk
+// copy issued by the TMA warp.  Every wait is bounded.
 #include <cmath>
 #include <cstdio>
 
@@ -32,71 +36,81 @@
 namespace kvc {
 namespace {
 
-constexpr int kEpiWarps = 8;                    // two warpgroups
+constexpr int kEpiWarps = 8;                    // two warpgroups, one per A tile
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // + TMA warp + MMA warp
-constexpr int BM = 128;        // A-operand rows (TMEM lanes)
+constexpr int BM = 128;        // A-operand rows per tile (TMEM lanes)
 constexpr int BN = 128;        // B-operand rows per chunk (TMEM columns)
-constexpr int kStages = 4;     // B ring depth
-constexpr int kAccCols = 2 * BN;  // two accumulators
+constexpr int kTiles = 2;      // A tiles per work item
+constexpr int kMaxStages = 4;  // B ring depth limit
+constexpr int kAccCols = 2 * kTiles * BN;  // accumulators: tile x parity = 512 columns
 
 struct Params {
-  int U, T, R, W, B, H;
-  int n_items, n_tiles, r_local;  // r_local: rows of row constants per buffer
+  int U, T, R, Rp, W, B, H;
+  int n_items, n_tiles, n_pairs, n_stages;
   float scale_log2;
   const int32_t* pad;
-  float2* rowpart;   // [2][U][R] per-warpgroup row statistics
-  float* usage;      // [2][U][T] per-warpgroup slot sums
+  float* negb;    // [U][Rp] -b_r (pass 1 writes, pass 2 reads by bulk copy)
+  float* pmax;    // [U][Rp] 1/Z'_r
+  float* usage;   // [U][T]
   uint32_t* status;
 };
 
 struct Item {
-  int u, tile, pad, n_ch, a_row, b_row0, c_start;
+  int u, pad, n_ch, c_start;
+  int tile[kTiles];   // tile index within the unit, -1 if absent
+  int a_row[kTiles];  // first A row of the tile in the 2-D tensor view
+  int b_row0;         // first B row of chunk 0
+  int n_present;
 };
 
 template <int PASS>
 __device__ __forceinline__ Item decode(const Params& p, int item) {
   Item it;
-  it.u = item / p.n_tiles;
-  it.tile = item - it.u * p.n_tiles;
+  it.u = item / p.n_pairs;
+  const int pair = item - it.u * p.n_pairs;
   const int b = (it.u / p.H) % p.B;
   it.pad = min(max(p.pad[b], 0), p.T);
+  it.n_present = 0;
+#pragma unroll
+  for (int t = 0; t < kTiles; ++t) {
+    const int tile = pair * kTiles + t;
+    bool present = tile < p.n_tiles;
+    if (PASS == 2) present = present && (tile * BM + BM > it.pad);  // not all padding
+    it.tile[t] = present ? tile : -1;
+    it.a_row[t] = (PASS == 1) ? it.u * p.R + tile * BM : it.u * p.T + tile * BM;
+    it.n_present += present ? 1 : 0;
+  }
   if (PASS == 1) {
     it.c_start = (it.pad / BN) * BN;
-    it.n_ch = (it.pad < p.T) ? (p.T - it.c_start + BN - 1) / BN : 0;
-    it.a_row = it.u * p.R + it.tile * BM;
+    it.n_ch = (it.pad < p.T && it.n_present) ? (p.T - it.c_start + BN - 1) / BN : 0;
     it.b_row0 = it.u * p.T + it.c_start;
   } else {
-    const int p0 = it.tile * BM;
     it.c_start = 0;
-    it.n_ch = (p0 + BM > it.pad && it.pad < p.T) ? (p.R + BN - 1) / BN : 0;
-    it.a_row = it.u * p.T + p0;
+    it.n_ch = (it.pad < p.T && it.n_present) ? (p.R + BN - 1) / BN : 0;
     it.b_row0 = it.u * p.R;
   }
   return it;
 }
 
-template <int D>
+// Shared-memory layout (byte offsets from the 1024-aligned base).
 struct Layout {
-  static constexpr int kKB = D / 64;               // 64-element (128 B) K blocks
-  static constexpr int kABytes = BM * D * 2;
-  static constexpr int kBBytes = BN * D * 2;
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = 2 * kABytes;
-  static constexpr int kOffBars = kOffB + kStages * kBBytes;
-  static constexpr int kNumBars = 2 * kStages + 6 + 1 + 4;
-  static_assert(kNumBars <= 24, "barrier area holds 24 barriers");
-  static constexpr int kOffMisc = kOffBars + 24 * 8;
-  static constexpr int kOffRowB = kOffMisc + 16;   // pass 2: row constants [2 wg][2 buf]
-  static size_t bytes(int r_local) {
-    return 1024 + kOffRowB + 4 * static_cast<size_t>(r_local) * 4;
+  int a_bytes, b_bytes, kb;  // per tile / per stage, 64-element K blocks
+  int off_b, off_bars, off_misc, off_rowb, total;
+  __host__ __device__ Layout(int D, int n_stages, int rowb_floats) {
+    kb = D / 64;
+    a_bytes = BM * D * 2;
+    b_bytes = BN * D * 2;
+    off_b = 2 * kTiles * a_bytes;  // A: [2 items][2 tiles]
+    off_bars = off_b + n_stages * b_bytes;
+    off_misc = off_bars + 32 * 8;
+    off_rowb = off_misc + 16;
+    total = 1024 + off_rowb + 2 * rowb_floats * 4;
   }
 };
 
-// Rows of row constants one warpgroup holds per item: its share of the chunks.
-__host__ __device__ inline int rows_local(int R) {
-  const int n_ch = (R + BN - 1) / BN;
-  return ((n_ch + 1) / 2) * BN;
-}
+// Row constants one pass-2 buffer holds: all chunks' rows (padding = -inf).
+__host__ __device__ inline int rowb_floats(int R) { return ((R + BN - 1) / BN) * BN; }
+__host__ __device__ inline int round4(int R) { return (R + 3) & ~3; }
 
 // Warp-uniform wait for the epilogue warps: lane 0 waits, the result is
 // broadcast, so that the collective TMEM loads that follow run converged.
@@ -129,17 +143,14 @@ __device__ __forceinline__ float lds32(const float* ptr) {
   return v;
 }
 
-__device__ __forceinline__ void sts32(float* ptr, float v) {
-  asm volatile("st.shared.f32 [%0], %1;" ::"r"(smem_u32(ptr)), "f"(v) : "memory");
-}
-
-// Row normaliser b_r = log2 sum_i exp2(x_i) from the two warpgroups' partial
-// (max, sum) pairs (x = scaled logits); +inf for a row that sees nothing.
-__device__ __forceinline__ float combine_row_b(float2 a, float2 b) {
-  const float m = fmaxf(a.x, b.x);
-  if (m == -INFINITY) return INFINITY;
-  const float s = a.y * ex2(a.x - m) + b.y * ex2(b.x - m);
-  return s > 0.f ? m + log2f(s) : INFINITY;
+// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 template <int D, int PASS>
@@ -147,45 +158,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     usage_kernel(const __grid_constant__ CUtensorMap map_a,
                  const __grid_constant__ CUtensorMap map_b, Params p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
-  using Ly = Layout<D>;
+  const int rbf = (PASS == 2) ? rowb_floats(p.R) : 0;
+  const Layout ly(D, p.n_stages, rbf);
+  const int NS = p.n_stages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle, as an offset from the shared
   // array so that the compiler keeps the shared address space
   const uint32_t mis = smem_u32(smem_raw) & 1023u;
   uint8_t* smem = smem_raw + ((1024u - mis) & 1023u);
-  uint8_t* a_buf = smem + Ly::kOffA;
-  uint8_t* b_buf = smem + Ly::kOffB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::kOffBars);
-  uint64_t* full = bars;                  // [kStages]
-  uint64_t* empty = bars + kStages;       // [kStages]
-  uint64_t* afull = bars + 2 * kStages;   // [2]
-  uint64_t* aempty = afull + 2;           // [2]
-  uint64_t* accfull = aempty + 2;         // [2]
-  uint64_t* accempty = accfull + 2;       // [2] (one arrival per epilogue warp)
-  uint64_t* done = accempty + 2;          // [1]
-  uint64_t* rb_full = done + 1;           // [2 wg][2 buf] row constants written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Ly::kOffMisc);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + Ly::kOffMisc + 4);
-  float* row_b_all = reinterpret_cast<float*>(smem + Ly::kOffRowB);
+  uint8_t* a_buf = smem;
+  uint8_t* b_buf = smem + ly.off_b;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ly.off_bars);
+  uint64_t* full = bars;                // [kMaxStages]
+  uint64_t* empty = bars + 4;           // [kMaxStages]
+  uint64_t* afull = bars + 8;           // [2]
+  uint64_t* aempty = bars + 10;         // [2]
+  uint64_t* accfull = bars + 12;        // [4]  tile * 2 + parity
+  uint64_t* accempty = bars + 16;       // [4]  (one arrival per warp of the tile's group)
+  uint64_t* done = bars + 20;           // [1]
+  uint64_t* rbfull = bars + 21;         // [2]  pass 2 row constants landed
+  uint64_t* rbempty = bars + 23;        // [2]  pass 2 row constants consumed (8 warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ly.off_misc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + ly.off_misc + 4);
+  float* row_b_all = reinterpret_cast<float*>(smem + ly.off_rowb);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&afull[b], 1);
       mbar_init(&aempty[b], 1);
-      mbar_init(&accfull[b], 1);
-      mbar_init(&accempty[b], 4);
+      mbar_init(&rbfull[b], 1);
+      mbar_init(&rbempty[b], kEpiWarps);
+    }
+    for (int a = 0; a < 4; ++a) {
+      mbar_init(&accfull[a], 1);
+      mbar_init(&accempty[a], 4);
     }
     mbar_init(done, 1);
-    for (int b = 0; b < 4; ++b) mbar_init(&rb_full[b], 128);
     *abort = 0;
     fence_barrier_init();
     prefetch_tensormap(&map_a);
     prefetch_tensormap(&map_b);
+  }
+  if constexpr (PASS == 2) {
+    // rows past the unit's constants never get copied: they must contribute 0
+    for (int i = threadIdx.x; i < 2 * rbf; i += kThreads) {
+      const int r = i % rbf;
+      if (r >= p.Rp) row_b_all[i] = -INFINITY;
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, kAccCols);
   tc_fence_before();
@@ -196,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int a_iter = 0, b_iter = 0;
+      int a_iter = 0, b_iter = 0, rb_iter = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
         const Item it = decode<PASS>(p, item);
@@ -207,29 +231,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ++a_iter;
-        mbar_arrive_expect_tx(&afull[ab], Ly::kABytes);
-        for (int kb = 0; kb < Ly::kKB; ++kb)
-          tma_load_2d(a_buf + ab * Ly::kABytes + kb * BM * 128, &map_a, kb * 64,
-                      it.a_row, &afull[ab]);
+        mbar_arrive_expect_tx(&afull[ab], it.n_present * ly.a_bytes);
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+          if (it.tile[t] < 0) continue;
+          for (int kb = 0; kb < ly.kb; ++kb)
+            tma_load_2d(a_buf + (ab * kTiles + t) * ly.a_bytes + kb * BM * 128, &map_a,
+                        kb * 64, it.a_row[t], &afull[ab]);
+        }
+        if (PASS == 2) {
+          const int rb = rb_iter & 1;
+          if (!mbar_wait(&rbempty[rb], ((rb_iter >> 1) & 1) ^ 1, abort, p.status)) {
+            ok = false;
+            break;
+          }
+          ++rb_iter;
+          mbar_arrive_expect_tx(&rbfull[rb], p.Rp * 4);
+          bulk_load(row_b_all + rb * rbf, p.negb + static_cast<size_t>(it.u) * p.Rp,
+                    p.Rp * 4, &rbfull[rb]);
+        }
         for (int c = 0; c < it.n_ch; ++c) {
-          const int s = b_iter % kStages;
-          if (!mbar_wait(&empty[s], ((b_iter / kStages) & 1) ^ 1, abort,
-                         p.status)) {
+          const int s = b_iter % NS;
+          if (!mbar_wait(&empty[s], ((b_iter / NS) & 1) ^ 1, abort, p.status)) {
             ok = false;
             break;
           }
           ++b_iter;
-          mbar_arrive_expect_tx(&full[s], Ly::kBBytes);
-          for (int kb = 0; kb < Ly::kKB; ++kb)
-            tma_load_2d(b_buf + s * Ly::kBBytes + kb * BN * 128, &map_b,
-                        kb * 64, it.b_row0 + c * BN, &full[s]);
+          mbar_arrive_expect_tx(&full[s], ly.b_bytes);
+          for (int kb = 0; kb < ly.kb; ++kb)
+            tma_load_2d(b_buf + s * ly.b_bytes + kb * BN * 128, &map_b, kb * 64,
+                        it.b_row0 + c * BN, &full[s]);
         }
       }
-      // drain: every issued load must land before the CTA may exit
-      for (int i = (b_iter > kStages ? b_iter - kStages : 0); i < b_iter; ++i)
-        drain_wait(&full[i % kStages], (i / kStages) & 1, p.status);
+      // drain: every issued copy must land before the CTA may exit
+      for (int i = (b_iter > NS ? b_iter - NS : 0); i < b_iter; ++i)
+        drain_wait(&full[i % NS], (i / NS) & 1, p.status);
       for (int i = (a_iter > 2 ? a_iter - 2 : 0); i < a_iter; ++i)
         drain_wait(&afull[i & 1], (i >> 1) & 1, p.status);
+      for (int i = (rb_iter > 2 ? rb_iter - 2 : 0); i < rb_iter; ++i)
+        drain_wait(&rbfull[i & 1], (i >> 1) & 1, p.status);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -237,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       const uint32_t a_base = smem_u32(a_buf), b_base = smem_u32(b_buf);
-      int a_iter = 0, b_iter = 0, acc_iter = 0;
+      int a_iter = 0, b_iter = 0;
+      int kt[kTiles] = {0, 0};  // accumulators filled per tile
       bool ok = true;
       for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
         const Item it = decode<PASS>(p, item);
@@ -248,29 +289,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ++a_iter;
-        for (int c = 0; c < it.n_ch; ++c) {
-          const int acc = acc_iter & 1;
-          const int s = b_iter % kStages;
-          if (!mbar_wait(&accempty[acc], ((acc_iter >> 1) & 1) ^ 1, abort,
-                         p.status) ||
-              !mbar_wait(&full[s], (b_iter / kStages) & 1, abort, p.status)) {
+        for (int c = 0; ok && c < it.n_ch; ++c) {
+          const int s = b_iter % NS;
+          if (!mbar_wait(&full[s], (b_iter / NS) & 1, abort, p.status)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t a_tile = a_base + ab * Ly::kABytes;
-          const uint32_t b_tile = b_base + s * Ly::kBBytes;
+          const uint32_t b_tile = b_base + s * ly.b_bytes;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const int kb = k / 4, kk = k % 4;
-            const uint64_t ad = sw128_desc(a_tile + kb * BM * 128 + kk * 32);
-            const uint64_t bd = sw128_desc(b_tile + kb * BN * 128 + kk * 32);
-            mma_bf16(tmem + acc * BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+          for (int t = 0; t < kTiles; ++t) {
+            if (it.tile[t] < 0) continue;
+            const int acc = t * 2 + (kt[t] & 1);
+            if (!mbar_wait(&accempty[acc], ((kt[t] >> 1) & 1) ^ 1, abort, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_tile = a_base + (ab * kTiles + t) * ly.a_bytes;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const int kb = k / 4, kk = k % 4;
+              const uint64_t ad = sw128_desc(a_tile + kb * BM * 128 + kk * 32);
+              const uint64_t bd = sw128_desc(b_tile + kb * BN * 128 + kk * 32);
+              mma_bf16(tmem + acc * BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&accfull[acc]);
+            ++kt[t];
           }
+          if (!ok) break;
           mma_commit(&empty[s]);
-          mma_commit(&accfull[acc]);
           ++b_iter;
-          ++acc_iter;
         }
         if (ok) mma_commit(&aempty[ab]);
       }
@@ -280,27 +328,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wg = (warp - 2) >> 2;   // warpgroup: accumulators of parity wg
+    const int wg = (warp - 2) >> 2;   // warpgroup = A tile slot of the item
     const int quarter = warp & 3;     // TMEM lane quarter this warp may access
     const int lrow = quarter * 32 + lane;
-    const uint32_t t_acc =
-        tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * BN;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float c = p.scale_log2;
-    int k_iter = 0;   // accumulators consumed by this warpgroup
-    int g = 0;        // global chunk index of the item's first chunk
+    int k = 0;        // accumulators of this tile slot consumed
     int rb_iter = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
       const Item it = decode<PASS>(p, item);
-      const int first = (wg - g) & 1;   // first chunk of this item that is ours
-      g += it.n_ch;
+      const int tile = it.tile[wg];
       if (PASS == 1) {
-        const int r = it.tile * BM + lrow;
+        const int r = (tile >= 0 ? tile : 0) * BM + lrow;
         const int qpos = p.T - p.W + (r % p.W);
-        const bool row_valid = (r < p.R) && (qpos >= it.pad) && (it.n_ch > 0);
+        const bool row_valid = tile >= 0 && (r < p.R) && (qpos >= it.pad) && (it.n_ch > 0);
         float mz = -INFINITY, sum = 0.f;  // max in raw logit units, sum rel. to it
-        for (int ch = first; ch < it.n_ch; ch += 2) {
-          if (!epi_wait(&accfull[wg], k_iter & 1, abort, p.status, lane)) {
+        for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
+          const int acc = wg * 2 + (k & 1);
+          if (!epi_wait(&accfull[acc], (k >> 1) & 1, abort, p.status, lane)) {
             ok = false;
             break;
           }
@@ -309,40 +355,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int lo = max(it.pad, c0), hi = min(qpos, c0 + BN - 1);
           const bool fast = __all_sync(0xffffffffu,
                                        row_valid && lo == c0 && hi == c0 + BN - 1);
-#pragma unroll 1
-          for (int bt = 0; bt < BN / 32; ++bt) {
-            uint32_t v[32];
-            __syncwarp();
-            tmem_ld32(t_acc + bt * 32, v);
-            tmem_ld_wait();
-            if (fast) {
-              float bm0 = __uint_as_float(v[0]), bm1 = __uint_as_float(v[1]);
+          // the whole 128-column accumulator row into registers, then release it
+          uint32_t v[BN / 32][32];
+          float bmx[BN / 32];
+          __syncwarp();
+          const uint32_t ta = t_lane + acc * BN;
+          if (fast) {
 #pragma unroll
-              for (int i = 2; i < 32; i += 2) {
-                bm0 = fmaxf(bm0, __uint_as_float(v[i]));
-                bm1 = fmaxf(bm1, __uint_as_float(v[i + 1]));
-              }
-              const float bm = fmaxf(bm0, bm1);
-              if (bm > mz) {
-                sum *= ex2((mz - bm) * c);
-                mz = bm;
-              }
-              const float neg = -mz * c;
-              float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            for (int bt = 0; bt < BN / 32; ++bt)
+              tmem_ld32_max(ta + bt * 32, v[bt], bmx[bt]);  // row max from the load path
+          } else {
+#pragma unroll
+            for (int bt = 0; bt < BN / 32; ++bt) tmem_ld32(ta + bt * 32, v[bt]);
+          }
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[acc]);
+          ++k;
+          if (fast) {
+            const float bm = fmaxf(fmaxf(bmx[0], bmx[1]), fmaxf(bmx[2], bmx[3]));
+            if (bm > mz) {
+              sum *= ex2((mz - bm) * c);
+              mz = bm;
+            }
+            const float neg = -mz * c;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int bt = 0; bt < BN / 32; ++bt) {
 #pragma unroll
               for (int i = 0; i < 32; i += 4) {
-                s0 += ex2(fmaf(__uint_as_float(v[i]), c, neg));
-                s1 += ex2(fmaf(__uint_as_float(v[i + 1]), c, neg));
-                s2 += ex2(fmaf(__uint_as_float(v[i + 2]), c, neg));
-                s3 += ex2(fmaf(__uint_as_float(v[i + 3]), c, neg));
+                float x0, x1, x2, x3;
+                fma2(x0, x1, __uint_as_float(v[bt][i]), __uint_as_float(v[bt][i + 1]), c, c,
+                     neg, neg);
+                fma2(x2, x3, __uint_as_float(v[bt][i + 2]), __uint_as_float(v[bt][i + 3]), c,
+                     c, neg, neg);
+                add2(s0, s1, s0, s1, ex2(x0), ex2(x1));
+                add2(s2, s3, s2, s3, ex2(x2), ex2(x3));
               }
-              sum += (s0 + s1) + (s2 + s3);
-            } else if (row_valid) {
+            }
+            sum += (s0 + s1) + (s2 + s3);
+          } else if (row_valid) {
+#pragma unroll
+            for (int bt = 0; bt < BN / 32; ++bt) {
               const int p0 = c0 + bt * 32;
               float bm = -INFINITY;
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (p0 + i >= lo && p0 + i <= hi) bm = fmaxf(bm, __uint_as_float(v[i]));
+                if (p0 + i >= lo && p0 + i <= hi) bm = fmaxf(bm, __uint_as_float(v[bt][i]));
               if (bm > mz) {
                 sum *= ex2((mz - bm) * c);
                 mz = bm;
@@ -352,72 +412,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 if (p0 + i >= lo && p0 + i <= hi)
-                  s0 += ex2(fmaf(__uint_as_float(v[i]), c, neg));
+                  s0 += ex2(fmaf(__uint_as_float(v[bt][i]), c, neg));
               sum += s0;
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[wg]);
-          ++k_iter;
         }
         if (!ok) break;
-        if (r < p.R) {
-          const float2 st = (row_valid && sum > 0.f) ? make_float2(mz * c, sum)
-                                                     : make_float2(-INFINITY, 0.f);
-          p.rowpart[(static_cast<size_t>(wg) * p.U + it.u) * p.R + r] = st;
+        if (tile >= 0 && r < p.Rp) {
+          const bool has = row_valid && sum > 0.f;
+          const size_t o = static_cast<size_t>(it.u) * p.Rp + r;
+          p.negb[o] = has ? -(mz * c + log2f(sum)) : -INFINITY;
+          p.pmax[o] = has ? 1.0f / sum : 0.f;
         }
       } else {
         if (it.n_ch == 0) continue;
-        // Row constants of the chunks this warpgroup takes, double buffered
-        // across items: every thread of the warpgroup writes its share and
-        // arrives; a thread only rewrites a buffer after the whole warpgroup
-        // arrived for the following item, i.e. finished with it.
+        // the unit's negated row constants (bulk copy by the TMA warp)
         const int rb = rb_iter & 1;
-        float* row_b = row_b_all + (wg * 2 + rb) * p.r_local;
-        {
-          int l = 0;
-          for (int ch = first; ch < it.n_ch; ch += 2, ++l) {
-            const int r = ch * BN + lrow;
-            float bv = INFINITY;
-            if (r < p.R) {
-              const size_t o = static_cast<size_t>(it.u) * p.R + r;
-              bv = combine_row_b(p.rowpart[o],
-                                 p.rowpart[static_cast<size_t>(p.U) * p.R + o]);
-            }
-            sts32(row_b + l * BN + lrow, bv);
-          }
-        }
-        mbar_arrive(&rb_full[wg * 2 + rb]);
-        if (!mbar_wait(&rb_full[wg * 2 + rb], (rb_iter >> 1) & 1, abort, p.status)) break;
+        if (!epi_wait(&rbfull[rb], (rb_iter >> 1) & 1, abort, p.status, lane)) break;
         ++rb_iter;
-        const int pos = it.tile * BM + lrow;
-        const bool pos_valid = (pos >= it.pad) && (pos < p.T);
+        const float* row_b = row_b_all + rb * rbf;
+        const int pos = (tile >= 0 ? tile : 0) * BM + lrow;
+        const bool pos_valid = tile >= 0 && (pos >= it.pad) && (pos < p.T);
         const bool fast = __all_sync(0xffffffffu, pos_valid && (pos <= p.T - p.W));
         const int jmin = pos - (p.T - p.W);  // rows with j >= jmin see pos
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        int l = 0;
-        for (int ch = first; ch < it.n_ch; ch += 2, ++l) {
-          if (!epi_wait(&accfull[wg], k_iter & 1, abort, p.status, lane)) {
+        for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
+          const int acc = wg * 2 + (k & 1);
+          if (!epi_wait(&accfull[acc], (k >> 1) & 1, abort, p.status, lane)) {
             ok = false;
             break;
           }
           tc_fence_after();
-#pragma unroll 1
+          uint32_t v[BN / 32][32];
+          __syncwarp();
+          const uint32_t ta = t_lane + acc * BN;
+#pragma unroll
+          for (int bt = 0; bt < BN / 32; ++bt) tmem_ld32(ta + bt * 32, v[bt]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[acc]);
+          ++k;
+#pragma unroll
           for (int bt = 0; bt < BN / 32; ++bt) {
-            uint32_t v[32];
-            __syncwarp();
-            tmem_ld32(t_acc + bt * 32, v);
-            tmem_ld_wait();
-            const float* rbb = row_b + l * BN + bt * 32;
+            const float* rbb = row_b + ch * BN + bt * 32;
             if (fast) {
 #pragma unroll
               for (int i = 0; i < 32; i += 4) {
-                const float4 bb = lds128(rbb + i);
-                a0 += ex2(fmaf(__uint_as_float(v[i]), c, -bb.x));
-                a1 += ex2(fmaf(__uint_as_float(v[i + 1]), c, -bb.y));
-                a2 += ex2(fmaf(__uint_as_float(v[i + 2]), c, -bb.z));
-                a3 += ex2(fmaf(__uint_as_float(v[i + 3]), c, -bb.w));
+                const float4 nb = lds128(rbb + i);  // negated row constants
+                float x0, x1, x2, x3;
+                fma2(x0, x1, __uint_as_float(v[bt][i]), __uint_as_float(v[bt][i + 1]), c, c,
+                     nb.x, nb.y);
+                fma2(x2, x3, __uint_as_float(v[bt][i + 2]), __uint_as_float(v[bt][i + 3]), c,
+                     c, nb.z, nb.w);
+                add2(a0, a1, a0, a1, ex2(x0), ex2(x1));
+                add2(a2, a3, a2, a3, ex2(x2), ex2(x3));
               }
             } else if (pos_valid) {
               const int r0 = ch * BN + bt * 32;
@@ -425,19 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 if (j >= jmin && r0 + i < p.R)
-                  a0 += ex2(fmaf(__uint_as_float(v[i]), c, -lds32(rbb + i)));
+                  a0 += ex2(fmaf(__uint_as_float(v[bt][i]), c, lds32(rbb + i)));
                 j = (j + 1 == p.W) ? 0 : j + 1;
               }
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[wg]);
-          ++k_iter;
         }
+        // every epilogue warp releases the row constants, tile or no tile
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rbempty[rb]);
         if (!ok) break;
         if (pos_valid)
-          p.usage[(static_cast<size_t>(wg) * p.U + it.u) * p.T + pos] = (a0 + a1) + (a2 + a3);
+          p.usage[static_cast<size_t>(it.u) * p.T + pos] = (a0 + a1) + (a2 + a3);
       }
     }
   }
@@ -474,16 +522,15 @@ EncodeTiledFn get_encode(std::string* err) {
 }
 
 // 2-D view [rows][d] of a bf16 tensor, boxes of 64 x 128 elements, 128 B swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int d,
-              std::string* err) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int d, std::string* err) {
   EncodeTiledFn enc = get_encode(err);
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), rows};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
-                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
@@ -491,6 +538,24 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int d,
     return false;
   }
   return true;
+}
+
+int smem_optin() {
+  static int v = 0;
+  if (!v) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      v = 227 * 1024;
+  }
+  return v;
+}
+
+// Deepest B ring (<= kMaxStages) that fits the shared memory; 0 if none fits.
+int pick_stages(int D, int rbf) {
+  for (int s = kMaxStages; s >= 2; --s)
+    if (Layout(D, s, rbf).total <= smem_optin()) return s;
+  return 0;
 }
 
 template <int D>
@@ -506,36 +571,38 @@ cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStre
   p.U = dm.U;
   p.T = a.T;
   p.R = dm.R;
+  p.Rp = round4(dm.R);
   p.W = dm.W;
   p.B = dm.B;
   p.H = dm.H;
   p.scale_log2 = a.scale_log2;
   p.pad = a.pad;
-  p.rowpart = h->ws.rowstat;
+  p.negb = h->ws.negb;
+  p.pmax = h->ws.pmax;
   p.usage = h->ws.usage;
-  p.r_local = rows_local(dm.R);
   p.status = h->ws.status;
 
+  const int rbf = (pass == 2) ? rowb_floats(dm.R) : 0;
+  p.n_stages = pick_stages(D, rbf);
+  if (p.n_stages == 0) {
+    if (err) *err = "attention kernel does not fit in shared memory";
+    return cudaErrorInvalidValue;
+  }
+  const size_t smem = Layout(D, p.n_stages, rbf).total;
+  p.n_tiles = (pass == 1) ? (dm.R + BM - 1) / BM : (a.T + BM - 1) / BM;
+  p.n_pairs = (p.n_tiles + kTiles - 1) / kTiles;
+  p.n_items = dm.U * p.n_pairs;
+  const int grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
   cudaError_t e;
   if (pass == 1) {
-    // items = (unit, 128-row tile)
-    const size_t smem = Layout<D>::bytes(0);
     e = cudaFuncSetAttribute(usage_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    p.n_tiles = (dm.R + BM - 1) / BM;
-    p.n_items = dm.U * p.n_tiles;
-    const int grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
     usage_kernel<D, 1><<<grid, kThreads, smem, s>>>(map_q, map_k, p);
   } else {
-    // items = (unit, 128-slot tile)
-    const size_t smem = Layout<D>::bytes(p.r_local);
     e = cudaFuncSetAttribute(usage_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    p.n_tiles = (a.T + BM - 1) / BM;
-    p.n_items = dm.U * p.n_tiles;
-    const int grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
     usage_kernel<D, 2><<<grid, kThreads, smem, s>>>(map_k, map_q, p);
   }
   return cudaGetLastError();
@@ -556,9 +623,11 @@ cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a, int 
   }
 }
 
+// Shared memory the attention kernels need with their shallowest ring (2 stages).
 size_t attention_usage_smem_bytes(int d, int R) {
-  const int rl = rows_local(R);
-  return d == 64 ? Layout<64>::bytes(rl) : Layout<128>::bytes(rl);
+  return static_cast<size_t>(Layout(d, 2, rowb_floats(R)).total);
 }
+
+int attention_row_stride(int R) { return round4(R); }
 
 }  // namespace kvc

@@ -10,6 +10,7 @@
 
 namespace kvc {
 size_t attention_usage_smem_bytes(int d, int R);
+int attention_row_stride(int R);
 size_t segment_smem_bytes(const kvc_config& c, int T);
 size_t select_smem_bytes(const kvc_config& c, int T);
 }  // namespace kvc
@@ -274,7 +275,7 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
     return KVC_ERR_UNSUPPORTED;
   }
 
-  const size_t U = d.U, T = cfg->max_T, R = d.R;
+  const size_t U = d.U, T = cfg->max_T;
   const size_t S = kvc::s_max_of(*cfg, cfg->max_T);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -282,8 +283,10 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
     off = align_up(off + bytes);
     return at;
   };
-  const size_t o_row = take(2 * U * R * sizeof(float2));  // two warpgroup halves
-  const size_t o_use = take(2 * U * T * 4);
+  const size_t Rp = kvc::attention_row_stride(d.R);
+  const size_t o_negb = take(U * Rp * 4);
+  const size_t o_pmax = take(U * Rp * 4);
+  const size_t o_use = take(U * T * 4);
   const size_t o_mass = take(U * T * 4);
   const size_t o_score = take(U * T * 4);
   const size_t o_cp = take(U * T * 4);
@@ -308,7 +311,8 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
   kvc::Workspace& w = h->ws;
   w.base = base;
   w.bytes = off;
-  w.rowstat = reinterpret_cast<float2*>(p + o_row);
+  w.negb = reinterpret_cast<float*>(p + o_negb);
+  w.pmax = reinterpret_cast<float*>(p + o_pmax);
   w.usage = reinterpret_cast<float*>(p + o_use);
   w.mass = reinterpret_cast<float*>(p + o_mass);
   w.score = reinterpret_cast<float*>(p + o_score);

@@ -18,8 +18,9 @@ namespace kvc {
 // ---------------------------------------------------------------- handle ----
 
 struct Workspace {
-  float2* rowstat = nullptr;    // [2][U][R] partial row stats {scaled max, sum}
-  float* usage = nullptr;       // [2][U][max_T] partial raw usage (no fill)
+  float* negb = nullptr;        // [U][Rp] -log2 row normaliser (Rp = R rounded to 4)
+  float* pmax = nullptr;        // [U][Rp] largest probability of each row
+  float* usage = nullptr;       // [U][max_T] raw usage (no fill)
   float* mass = nullptr;        // [U][max_T]   (event intermediates)
   float* score = nullptr;       // [U][max_T]
   float* credit_post = nullptr; // [U][max_T]
@@ -295,6 +296,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+
+// As tmem_ld32, and also the maximum of the 32 loaded fp32 values of the lane
+// (computed by the TMEM load path itself).
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32],
+                                              float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, "
+      "%32, [%33];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31]), "=f"(mx)
+      : "r"(taddr)
+      : "memory");
+}
+
+// Packed pair arithmetic (two fp32 lanes per instruction).
+__device__ __forceinline__ void fma2(float& dx, float& dy, float ax, float ay, float bx,
+                                     float by, float cx, float cy) {
+  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(dx), "=f"(dy)
+      : "f"(ax), "f"(ay), "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+
+__device__ __forceinline__ void add2(float& dx, float& dy, float ax, float ay, float bx,
+                                     float by) {
+  asm("{\n\t.reg .b64 a, b, d;\n\t"
+      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(dx), "=f"(dy)
+      : "f"(ax), "f"(ay), "f"(bx), "f"(by));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -20,6 +20,7 @@
 #include "kvc_internal.cuh"
 
 namespace kvc {
+int attention_row_stride(int R);
 namespace {
 
 constexpr int kThreads = 256;
@@ -63,10 +64,9 @@ struct PostParams {
   int T, R, W, G, B, H;
   int avg_pool, max_pool;
   float eps, lambda, beta;
-  int U;
-  const float2* rowstat;  // [2][U][R] partial (scaled max, sum) per row
-  float* usage;           // [2][U][T] partial raw usage; half 0 becomes the
-                          // filled usage in place
+  int Rp;
+  const float* pmax;  // [U][Rp] largest probability of each row (0 if absent)
+  float* usage;       // [U][T] raw usage, filled in place
   const int32_t* pad;
   const int32_t* n_carry;
   const float* credit_in;
@@ -98,26 +98,17 @@ __global__ void __launch_bounds__(kThreads)
     return;
   }
 
-  // fill value = largest probability of any present row: 1/Z'_r, Z'_r the
-  // row's exp-sum relative to its maximum (absent rows contribute 0)
+  // fill value = largest probability of any present row (absent rows hold 0)
   float pm = 0.f;
-  for (int r = threadIdx.x; r < p.R; r += kThreads) {
-    const size_t o = static_cast<size_t>(u) * p.R + r;
-    const float2 s0 = p.rowstat[o];
-    const float2 s1 = p.rowstat[static_cast<size_t>(p.U) * p.R + o];
-    const float m = fmaxf(s0.x, s1.x);
-    if (m == -INFINITY) continue;
-    const float z = s0.y * exp2f(s0.x - m) + s1.y * exp2f(s1.x - m);
-    if (z > 0.f) pm = fmaxf(pm, 1.0f / z);
-  }
+  for (int r = threadIdx.x; r < p.R; r += kThreads)
+    pm = fmaxf(pm, p.pmax[static_cast<size_t>(u) * p.Rp + r]);
   const float fill = block_max(pm, red);
-  const float* a_other = p.usage + static_cast<size_t>(p.U) * T + base;
 
   // a'(i) = a(i) + fill * (#present (head, query) pairs that cannot see i)
   const int j_lo = max(0, pad - (T - p.W));  // first present window query
   for (int i = pad + threadIdx.x; i < T; i += kThreads) {
     const int unseen = max(0, min(p.W, i - T + p.W) - j_lo) * p.G;
-    a[i] = (a[i] + a_other[i]) + fill * static_cast<float>(unseen);
+    a[i] += fill * static_cast<float>(unseen);
   }
   __syncthreads();
 
@@ -193,8 +184,8 @@ cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
   p.eps = h->cfg.eps;
   p.lambda = h->cfg.lambda;
   p.beta = h->cfg.beta;
-  p.U = dm.U;
-  p.rowstat = h->ws.rowstat;
+  p.Rp = attention_row_stride(dm.R);
+  p.pmax = h->ws.pmax;
   p.usage = h->ws.usage;
   p.pad = pad;
   p.n_carry = n_carry;
