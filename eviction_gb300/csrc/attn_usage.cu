@@ -46,7 +46,7 @@ constexpr int kAccCols = 2 * kTiles * BN;  // accumulators: tile x parity = 512 
 
 struct Params {
   int U, T, R, Rp, W, B, H;
-  int n_items, n_tiles, n_pairs, n_stages;
+  int n_items, n_tiles, n_pairs, n_stages, unit_major;
   float scale_log2;
   const int32_t* pad;
   float* negb;    // [U][Rp] -b_r (pass 1 writes, pass 2 reads by bulk copy)
@@ -153,6 +153,20 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// The k-th work item of this CTA, or -1 past the end.  With many units per SM
+// each CTA takes whole units (all tile pairs of a unit back to back): no two SMs
+// then fetch the same operand lines at the same moment, and the unit's operands
+// stay in L2 for the CTA's next items.  With few units, items are interleaved
+// across CTAs so that every SM has work.
+__device__ __forceinline__ int cta_item(const Params& p, int k) {
+  if (p.unit_major) {
+    const int unit = blockIdx.x + (k / p.n_pairs) * gridDim.x;
+    return unit < p.U ? unit * p.n_pairs + (k % p.n_pairs) : -1;
+  }
+  const int item = blockIdx.x + k * gridDim.x;
+  return item < p.n_items ? item : -1;
+}
+
 template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1)
     usage_kernel(const __grid_constant__ CUtensorMap map_a,
@@ -222,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int a_iter = 0, b_iter = 0, rb_iter = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
         if (it.n_ch == 0) continue;
         const int ab = a_iter & 1;
@@ -235,9 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kTiles; ++t) {
           if (it.tile[t] < 0) continue;
-          for (int kb = 0; kb < ly.kb; ++kb)
-            tma_load_2d(a_buf + (ab * kTiles + t) * ly.a_bytes + kb * BM * 128, &map_a,
-                        kb * 64, it.a_row[t], &afull[ab]);
+          // one box: 128 rows x all 64-element K blocks, K block outermost
+          tma_load_3d(a_buf + (ab * kTiles + t) * ly.a_bytes, &map_a, 0, it.a_row[t], 0,
+                      &afull[ab]);
+        }
+        // L2 prefetch of the next item's operands: the loads of CTAs that share
+        // a unit would otherwise all wait out the same DRAM fill
+        const int nxt = cta_item(p, kk + 1);
+        if (nxt >= 0) {
+          const Item nx = decode<PASS>(p, nxt);
+          if (nx.n_ch > 0) {
+#pragma unroll
+            for (int t = 0; t < kTiles; ++t)
+              if (nx.tile[t] >= 0) tma_prefetch_3d(&map_a, 0, nx.a_row[t], 0);
+            for (int c = 0; c < nx.n_ch; ++c) tma_prefetch_3d(&map_b, 0, nx.b_row0 + c * BN, 0);
+            if (PASS == 2)
+              bulk_prefetch_l2(p.negb + static_cast<size_t>(nx.u) * p.Rp, p.Rp * 4);
+          }
         }
         if (PASS == 2) {
           const int rb = rb_iter & 1;
@@ -258,9 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++b_iter;
           mbar_arrive_expect_tx(&full[s], ly.b_bytes);
-          for (int kb = 0; kb < ly.kb; ++kb)
-            tma_load_2d(b_buf + s * ly.b_bytes + kb * BN * 128, &map_b, kb * 64,
-                        it.b_row0 + c * BN, &full[s]);
+          tma_load_3d(b_buf + s * ly.b_bytes, &map_b, 0, it.b_row0 + c * BN, 0, &full[s]);
         }
       }
       // drain: every issued copy must land before the CTA may exit
@@ -280,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int a_iter = 0, b_iter = 0;
       int kt[kTiles] = {0, 0};  // accumulators filled per tile
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
         if (it.n_ch == 0) continue;
         const int ab = a_iter & 1;
@@ -336,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k = 0;        // accumulators of this tile slot consumed
     int rb_iter = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+    for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
       const Item it = decode<PASS>(p, item);
       const int tile = it.tile[wg];
       if (PASS == 1) {
@@ -521,15 +547,19 @@ EncodeTiledFn get_encode(std::string* err) {
   return fn;
 }
 
-// 2-D view [rows][d] of a bf16 tensor, boxes of 64 x 128 elements, 128 B swizzle.
+// 3-D view of a [rows][d] bf16 tensor: x = 64 elements of a K block (128 B),
+// y = row (stride d*2 B), z = K block (stride 128 B).  A box of 64 x 128 x d/64
+// lands in shared memory as d/64 consecutive [128 rows][128 B] blocks, each
+// with the 128-byte swizzle -- the K-major layout the MMA descriptors expect --
+// in a single TMA operation.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int d, std::string* err) {
   EncodeTiledFn enc = get_encode(err);
   if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), rows};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+  cuuint64_t dims[3] = {64, rows, static_cast<cuuint64_t>(d / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, 128};
+  cuuint32_t box[3] = {64, 128, static_cast<cuuint32_t>(d / 64)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -592,6 +622,7 @@ cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStre
   p.n_tiles = (pass == 1) ? (dm.R + BM - 1) / BM : (a.T + BM - 1) / BM;
   p.n_pairs = (p.n_tiles + kTiles - 1) / kTiles;
   p.n_items = dm.U * p.n_pairs;
+  p.unit_major = dm.U >= 2 * h->num_sms ? 1 : 0;
   const int grid = p.n_items < h->num_sms ? p.n_items : h->num_sms;
   cudaError_t e;
   if (pass == 1) {
