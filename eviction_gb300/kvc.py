@@ -19,7 +19,7 @@ _LIB_PATH = os.path.join(HERE, "libkvc.so")
 ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_sizes",
                 "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
                 "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
-                "kvc_profile_read")
+                "kvc_profile_read", "kvc_mass_noalloc")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -116,6 +116,8 @@ def load_library():
     L.kvc_last_error.restype = ctypes.c_char_p
     L.kvc_profile.argtypes = [_P, _I]
     L.kvc_profile_read.argtypes = [_P, ctypes.POINTER(_KernelTime), _I, ctypes.POINTER(_I), _I]
+    L.kvc_mass_noalloc.argtypes = [ctypes.POINTER(_CConfig), _P, _P, _I, _P, _P, _P, _P, _P, _P,
+                                   _P, _P]
     L.kvc_status_string.argtypes = [_I]
     L.kvc_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -143,6 +145,22 @@ def _dev(t, dtype, name):
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
+
+
+def mass_noalloc(cfg: Config, q, k, T, pad, n_carry, credit_in, credit_post, mass, score,
+                 status=None, stream=None) -> int:
+    """kvc_mass_noalloc: steps 1-2 without a handle and without any device
+    allocation (for callers that cannot allocate; see include/kvc.h).
+    Returns the library's status code (0 = KVC_OK)."""
+    import torch
+    c = cfg.c()
+    st = _dev(status, torch.int32, "status") if status is not None else ctypes.c_void_p(0)
+    return load_library().kvc_mass_noalloc(
+        ctypes.byref(c), _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), T,
+        _dev(pad, torch.int32, "pad"), _dev(n_carry, torch.int32, "n_carry"),
+        _dev(credit_in, torch.float32, "credit_in"), _dev(credit_post, torch.float32, "credit_post"),
+        _dev(mass, torch.float32, "mass"), _dev(score, torch.float32, "score"), st,
+        _stream_ptr(stream))
 
 
 class Handle:

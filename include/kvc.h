@@ -176,6 +176,30 @@ int kvc_profile(kvc_handle* h, int enable);
 int kvc_profile_read(kvc_handle* h, kvc_kernel_time* out, int capacity,
                      int* n_out, int reset);
 
+/* ---- no-allocation variant ----------------------------------------------
+ * No counterpart in the pages: this is a deployment aid.  kvc_mass_noalloc
+ * computes exactly what kvc_mass computes (same kernels, same results) for
+ * callers that cannot allocate device memory when they compress -- e.g. an
+ * engine that has reserved all free memory for its KV pool -- so it takes no
+ * handle and never allocates.  Its scratch is a fixed device array of
+ * KVC_NOALLOC_SCRATCH_FLOATS floats (4 MiB) that every GPU loading this
+ * library holds until the process exits; a call needs
+ * about n_layers*batch*n_kv_heads * (2*group*window + T) floats and returns
+ * KVC_ERR_SHAPE (with a message on stderr) above that -- call it per layer or
+ * on fewer sequences then.  The config fields kvc_mass uses are checked as in
+ * kvc_create; q, k, pad, n_carry, credit_in, credit_post, mass, score are as in
+ * kvc_mass.
+ * status: optional device uint32 the kernels OR their KVC_STATUS_* bits into
+ * (caller-zeroed); NULL uses a word in the scratch that each call clears.
+ * The first call on a device (with it current) looks up the scratch address
+ * with cudaGetSymbolAddress; make that first call before any stream capture.
+ * Every call shares the scratch: calls that overlap on the GPU race. */
+#define KVC_NOALLOC_SCRATCH_FLOATS (1u << 20)
+int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const uint16_t* k,
+                     int T, const int32_t* pad, const int32_t* n_carry,
+                     const float* credit_in, float* credit_post, float* mass,
+                     float* score, uint32_t* status, void* stream);
+
 /* Synchronise `stream`, then read and clear the device status bits. */
 int kvc_get_device_status(kvc_handle* h, uint32_t* bits, void* stream);
 
