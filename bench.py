@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qwen_28l")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="the same workload recipe cut to this many layers (small profiling case)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -186,6 +188,21 @@ def summarize_clocks(rows, t0, t1):
     return {"sm_mhz": statistics.median(r["sm"] for r in inside),
             "sm_max_mhz": max(r["sm_max"] for r in inside),
             "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+def reduce_over_ranks(elapsed_ms, tokens, device):
+    """(max elapsed over ranks, sum of tokens over ranks); identity on one rank.
+
+    Timing only: the ranks exchange two numbers, never any data of the event."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(elapsed_ms), float(tokens)
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
 
 
 def dist_env():
@@ -350,16 +367,7 @@ def run_ours(args, w):
     if status:
         raise RuntimeError(f"device status bits {status:#x} after the timed region")
 
-    total_tokens = tokens_per_step
-    max_ms = elapsed_ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        max_ms = float(t.item())
-        tt = torch.tensor([tokens_per_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.SUM)
-        total_tokens = float(tt.item())
+    max_ms, total_tokens = reduce_over_ranks(elapsed_ms, tokens_per_step, dev)
     ms_per_step = max_ms / args.steps
     value = total_tokens / (ms_per_step / 1000.0)
 
@@ -425,11 +433,7 @@ def run_ours(args, w):
         f1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = f0.elapsed_time(f1) / args.e2e_steps
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms, _ = reduce_over_ranks(e2e_ms, 0.0, dev)
         e2e = {"value": total_tokens / (e2e_ms / 1000.0), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": args.e2e_steps}
@@ -488,6 +492,8 @@ def main():
     args = parse_args()
     import workload as wl
     w = wl.CONFIGS[args.workload]
+    if args.layers:
+        w = wl.scaled(w, n_layers=args.layers, name=f"{w.name}_{args.layers}layers")
     if args.impl == "reference":
         world, rank, _ = dist_env()
         if rank != 0:
