@@ -41,12 +41,12 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;   // + TMA warp + MMA warp
 constexpr int BM = 128;        // A-operand rows per tile (TMEM lanes)
 constexpr int BN = 128;        // B-operand rows per chunk (TMEM columns)
 constexpr int kTiles = 2;      // A tiles per work item
-constexpr int kMaxStages = 4;  // B ring depth limit
+constexpr int kMaxStages = 6;  // B ring depth limit
 constexpr int kAccCols = 2 * kTiles * BN;  // accumulators: tile x parity = 512 columns
 
 struct Params {
   int U, T, R, Rp, W, B, H;
-  int n_items, n_tiles, n_pairs, n_stages, unit_major;
+  int n_items, n_tiles, n_pairs, n_stages, n_abuf, unit_major;
   float scale_log2;
   const int32_t* pad;
   float* negb;    // [U][Rp] -b_r (pass 1 writes, pass 2 reads by bulk copy)
@@ -96,11 +96,11 @@ __device__ __forceinline__ Item decode(const Params& p, int item) {
 struct Layout {
   int a_bytes, b_bytes, kb;  // per tile / per stage, 64-element K blocks
   int off_b, off_bars, off_misc, off_rowb, total;
-  __host__ __device__ Layout(int D, int n_stages, int rowb_floats) {
+  __host__ __device__ Layout(int D, int n_stages, int rowb_floats, int n_abuf) {
     kb = D / 64;
     a_bytes = BM * D * 2;
     b_bytes = BN * D * 2;
-    off_b = 2 * kTiles * a_bytes;  // A: [2 items][2 tiles]
+    off_b = n_abuf * kTiles * a_bytes;  // A: [n_abuf items][2 tiles]
     off_bars = off_b + n_stages * b_bytes;
     off_misc = off_bars + 32 * 8;
     off_rowb = off_misc + 16;
@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap map_b, Params p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
   const int rbf = (PASS == 2) ? rowb_floats(p.R) : 0;
-  const Layout ly(D, p.n_stages, rbf);
+  const Layout ly(D, p.n_stages, rbf, p.n_abuf);
+  const int NA = p.n_abuf;
   const int NS = p.n_stages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle, as an offset from the shared
@@ -183,15 +184,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* a_buf = smem;
   uint8_t* b_buf = smem + ly.off_b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ly.off_bars);
-  uint64_t* full = bars;                // [kMaxStages]
-  uint64_t* empty = bars + 4;           // [kMaxStages]
-  uint64_t* afull = bars + 8;           // [2]
-  uint64_t* aempty = bars + 10;         // [2]
-  uint64_t* accfull = bars + 12;        // [4]  tile * 2 + parity
-  uint64_t* accempty = bars + 16;       // [4]  (one arrival per warp of the tile's group)
-  uint64_t* done = bars + 20;           // [1]
-  uint64_t* rbfull = bars + 21;         // [2]  pass 2 row constants landed
-  uint64_t* rbempty = bars + 23;        // [2]  pass 2 row constants consumed (8 warps)
+  uint64_t* full = bars;                          // [kMaxStages]
+  uint64_t* empty = bars + kMaxStages;            // [kMaxStages]
+  uint64_t* afull = bars + 2 * kMaxStages;        // [2]
+  uint64_t* aempty = afull + 2;                   // [2]
+  uint64_t* accfull = aempty + 2;                 // [4]  tile * 2 + parity
+  uint64_t* accempty = accfull + 4;               // [4]  (one arrival per warp of the tile's group)
+  uint64_t* done = accempty + 4;                  // [1]
+  uint64_t* rbfull = done + 1;                    // [2]  pass 2 row constants landed
+  uint64_t* rbempty = rbfull + 2;                 // [2]  pass 2 row constants consumed (8 warps)
+  static_assert(2 * kMaxStages + 2 + 2 + 4 + 4 + 1 + 2 + 2 <= 32, "barrier area holds 32");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ly.off_misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + ly.off_misc + 4);
   float* row_b_all = reinterpret_cast<float*>(smem + ly.off_rowb);
@@ -239,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
         if (it.n_ch == 0) continue;
-        const int ab = a_iter & 1;
-        if (!mbar_wait(&aempty[ab], ((a_iter >> 1) & 1) ^ 1, abort, p.status)) {
+        const int ab = a_iter % NA;
+        if (!mbar_wait(&aempty[ab], ((a_iter / NA) & 1) ^ 1, abort, p.status)) {
           ok = false;
           break;
         }
@@ -292,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: every issued copy must land before the CTA may exit
       for (int i = (b_iter > NS ? b_iter - NS : 0); i < b_iter; ++i)
         drain_wait(&full[i % NS], (i / NS) & 1, p.status);
-      for (int i = (a_iter > 2 ? a_iter - 2 : 0); i < a_iter; ++i)
-        drain_wait(&afull[i & 1], (i >> 1) & 1, p.status);
+      for (int i = (a_iter > NA ? a_iter - NA : 0); i < a_iter; ++i)
+        drain_wait(&afull[i % NA], (i / NA) & 1, p.status);
       for (int i = (rb_iter > 2 ? rb_iter - 2 : 0); i < rb_iter; ++i)
         drain_wait(&rbfull[i & 1], (i >> 1) & 1, p.status);
     }
@@ -309,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
         if (it.n_ch == 0) continue;
-        const int ab = a_iter & 1;
-        if (!mbar_wait(&afull[ab], (a_iter >> 1) & 1, abort, p.status)) {
+        const int ab = a_iter % NA;
+        if (!mbar_wait(&afull[ab], (a_iter / NA) & 1, abort, p.status)) {
           ok = false;
           break;
         }
@@ -581,10 +583,12 @@ int smem_optin() {
   return v;
 }
 
-// Deepest B ring (<= kMaxStages) that fits the shared memory; 0 if none fits.
-int pick_stages(int D, int rbf) {
+// A buffers (items in flight) and B-ring depth: two A buffers (the next item's
+// operands load while the current item runs) with the deepest ring that fits.
+constexpr int kAbuf = 2;
+int pick_stages(int D, int rbf, int n_abuf) {
   for (int s = kMaxStages; s >= 2; --s)
-    if (Layout(D, s, rbf).total <= smem_optin()) return s;
+    if (Layout(D, s, rbf, n_abuf).total <= smem_optin()) return s;
   return 0;
 }
 
@@ -613,12 +617,13 @@ cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStre
   p.status = h->ws.status;
 
   const int rbf = (pass == 2) ? rowb_floats(dm.R) : 0;
-  p.n_stages = pick_stages(D, rbf);
+  p.n_abuf = kAbuf;
+  p.n_stages = pick_stages(D, rbf, p.n_abuf);
   if (p.n_stages == 0) {
     if (err) *err = "attention kernel does not fit in shared memory";
     return cudaErrorInvalidValue;
   }
-  const size_t smem = Layout(D, p.n_stages, rbf).total;
+  const size_t smem = Layout(D, p.n_stages, rbf, p.n_abuf).total;
   p.n_tiles = (pass == 1) ? (dm.R + BM - 1) / BM : (a.T + BM - 1) / BM;
   p.n_pairs = (p.n_tiles + kTiles - 1) / kTiles;
   p.n_items = dm.U * p.n_pairs;
@@ -656,7 +661,7 @@ cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a, int 
 
 // Shared memory the attention kernels need with their shallowest ring (2 stages).
 size_t attention_usage_smem_bytes(int d, int R) {
-  return static_cast<size_t>(Layout(d, 2, rowb_floats(R)).total);
+  return static_cast<size_t>(Layout(d, 2, rowb_floats(R), kAbuf).total);
 }
 
 int attention_row_stride(int R) { return round4(R); }
