@@ -21,13 +21,15 @@
 //           exp2(scale*log2e*z - b_r) over the rows.
 // Work item = one unit and a PAIR of 128-row A tiles: every B chunk that TMA
 // brings in feeds two MMAs (one per tile), which halves the operand traffic
-// per FLOP.  Persistent warp-specialised CTAs: warp 0 issues TMA loads (A
-// double-buffered across items, B through a ring), warp 1 issues tcgen05.mma
-// into four TMEM accumulators (tile x parity), warpgroup 0 (warps 2-5) drains
-// tile 0 and warpgroup 1 (warps 6-9) tile 1; each epilogue thread copies a
-// whole accumulator row to registers, hands the accumulator back, then
-// computes.  In pass 2 the row constants of the item's unit arrive by a bulk
-// copy issued by the TMA warp.  Every wait is bounded.
+// per FLOP.  Persistent warp-specialised CTAs: warp 0 streams B chunks
+// through a ring (TMA), warp 18 loads the A tiles (double-buffered across
+// items) and, in pass 2, the item's row constants (one bulk copy), warp 1
+// issues tcgen05.mma into four TMEM accumulators (tile x parity), and 16
+// epilogue warps (warps 2-17: tile slot x column half x lane quarter) drain
+// them: each copies its 32 rows x 64 columns of an accumulator to registers,
+// hands the accumulator back, then computes; the two column halves of a row
+// (pass 1) or slot (pass 2) are combined at the end of the item.  Every wait
+// is bounded.
 #include <cmath>
 #include <cstdio>
 
@@ -36,13 +38,15 @@
 namespace kvc {
 namespace {
 
-constexpr int kEpiWarps = 8;                    // two warpgroups, one per A tile
-constexpr int kThreads = 64 + 32 * kEpiWarps;   // + TMA warp + MMA warp
+constexpr int kEpiWarps = 16;                       // tile slot x column half x lane quarter
+constexpr int kLoaderWarp = 2 + kEpiWarps;          // A tiles / row constants
+constexpr int kThreads = 32 * (kLoaderWarp + 1);    // B warp, MMA warp, epilogue, loader
 constexpr int BM = 128;        // A-operand rows per tile (TMEM lanes)
 constexpr int BN = 128;        // B-operand rows per chunk (TMEM columns)
 constexpr int kTiles = 2;      // A tiles per work item
 constexpr int kMaxStages = 6;  // B ring depth limit
 constexpr int kAccCols = 2 * kTiles * BN;  // accumulators: tile x parity = 512 columns
+constexpr int kBarriers = 48;              // mbarrier slots in shared memory
 
 struct Params {
   int U, T, R, Rp, W, B, H;
@@ -102,7 +106,7 @@ struct Layout {
     b_bytes = BN * D * 2;
     off_b = n_abuf * kTiles * a_bytes;  // A: [n_abuf items][2 tiles]
     off_bars = off_b + n_stages * b_bytes;
-    off_misc = off_bars + 32 * 8;
+    off_misc = off_bars + kBarriers * 8;
     off_rowb = off_misc + 16;
     total = 1024 + off_rowb + 2 * rowb_floats * 4;
   }
@@ -134,12 +138,6 @@ __device__ __forceinline__ float4 lds128(const float* ptr) {
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "r"(smem_u32(ptr)));
-  return v;
-}
-
-__device__ __forceinline__ float lds32(const float* ptr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(ptr)));
   return v;
 }
 
@@ -189,11 +187,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* afull = bars + 2 * kMaxStages;        // [2]
   uint64_t* aempty = afull + 2;                   // [2]
   uint64_t* accfull = aempty + 2;                 // [4]  tile * 2 + parity
-  uint64_t* accempty = accfull + 4;               // [4]  (one arrival per warp of the tile's group)
+  uint64_t* accempty = accfull + 4;               // [4]  (one arrival per epilogue warp of the tile)
   uint64_t* done = accempty + 4;                  // [1]
   uint64_t* rbfull = done + 1;                    // [2]  pass 2 row constants landed
-  uint64_t* rbempty = rbfull + 2;                 // [2]  pass 2 row constants consumed (8 warps)
-  static_assert(2 * kMaxStages + 2 + 2 + 4 + 4 + 1 + 2 + 2 <= 32, "barrier area holds 32");
+  uint64_t* rbempty = rbfull + 2;                 // [2]  pass 2 row constants consumed (all epilogue warps)
+  uint64_t* mrg_full = rbempty + 2;               // [8]  half 1's partials stored (tile slot x quarter)
+  uint64_t* mrg_empty = mrg_full + 2 * 4;         // [8]  half 0 has read them
+  static_assert(2 * kMaxStages + 2 + 2 + 4 + 4 + 1 + 2 + 2 + 8 + 8 <= kBarriers,
+                "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ly.off_misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + ly.off_misc + 4);
   float* row_b_all = reinterpret_cast<float*>(smem + ly.off_rowb);
@@ -212,7 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 4; ++a) {
       mbar_init(&accfull[a], 1);
-      mbar_init(&accempty[a], 4);
+      mbar_init(&accempty[a], 8);  // 4 lane quarters x 2 column halves
+    }
+    for (int m = 0; m < 8; ++m) {
+      mbar_init(&mrg_full[m], 1);
+      mbar_init(&mrg_empty[m], 1);
     }
     mbar_init(done, 1);
     *abort = 0;
@@ -234,52 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ B producer
     if (lane == 0) {
-      int a_iter = 0, b_iter = 0, rb_iter = 0;
+      int b_iter = 0;
       bool ok = true;
       for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
-        if (it.n_ch == 0) continue;
-        const int ab = a_iter % NA;
-        if (!mbar_wait(&aempty[ab], ((a_iter / NA) & 1) ^ 1, abort, p.status)) {
-          ok = false;
-          break;
-        }
-        ++a_iter;
-        mbar_arrive_expect_tx(&afull[ab], it.n_present * ly.a_bytes);
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t) {
-          if (it.tile[t] < 0) continue;
-          // one box: 128 rows x all 64-element K blocks, K block outermost
-          tma_load_3d(a_buf + (ab * kTiles + t) * ly.a_bytes, &map_a, 0, it.a_row[t], 0,
-                      &afull[ab]);
-        }
-        // L2 prefetch of the next item's operands: the loads of CTAs that share
-        // a unit would otherwise all wait out the same DRAM fill
-        const int nxt = cta_item(p, kk + 1);
-        if (nxt >= 0) {
-          const Item nx = decode<PASS>(p, nxt);
-          if (nx.n_ch > 0) {
-#pragma unroll
-            for (int t = 0; t < kTiles; ++t)
-              if (nx.tile[t] >= 0) tma_prefetch_3d(&map_a, 0, nx.a_row[t], 0);
-            for (int c = 0; c < nx.n_ch; ++c) tma_prefetch_3d(&map_b, 0, nx.b_row0 + c * BN, 0);
-            if (PASS == 2)
-              bulk_prefetch_l2(p.negb + static_cast<size_t>(nx.u) * p.Rp, p.Rp * 4);
-          }
-        }
-        if (PASS == 2) {
-          const int rb = rb_iter & 1;
-          if (!mbar_wait(&rbempty[rb], ((rb_iter >> 1) & 1) ^ 1, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          ++rb_iter;
-          mbar_arrive_expect_tx(&rbfull[rb], p.Rp * 4);
-          bulk_load(row_b_all + rb * rbf, p.negb + static_cast<size_t>(it.u) * p.Rp,
-                    p.Rp * 4, &rbfull[rb]);
-        }
         for (int c = 0; c < it.n_ch; ++c) {
           const int s = b_iter % NS;
           if (!mbar_wait(&empty[s], ((b_iter / NS) & 1) ^ 1, abort, p.status)) {
@@ -294,6 +259,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: every issued copy must land before the CTA may exit
       for (int i = (b_iter > NS ? b_iter - NS : 0); i < b_iter; ++i)
         drain_wait(&full[i % NS], (i / NS) & 1, p.status);
+    }
+    __syncwarp();
+  } else if (warp == kLoaderWarp) {
+    // ------------------------------------------- A tiles and row constants
+    // Runs up to two items ahead of the MMA warp, independently of the B ring,
+    // so that an item's A tiles (and in pass 2 its row constants) have landed
+    // by the time its first B chunk arrives.
+    if (lane == 0) {
+      int a_iter = 0, rb_iter = 0;
+      bool ok = true;
+      for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
+        const Item it = decode<PASS>(p, item);
+        if (it.n_ch == 0) continue;
+        const int ab = a_iter % NA;
+        if (!mbar_wait(&aempty[ab], ((a_iter / NA) & 1) ^ 1, abort, p.status)) break;
+        ++a_iter;
+        mbar_arrive_expect_tx(&afull[ab], it.n_present * ly.a_bytes);
+#pragma unroll
+        for (int t = 0; t < kTiles; ++t) {
+          if (it.tile[t] < 0) continue;
+          // one box: 128 rows x all 64-element K blocks, K block outermost
+          tma_load_3d(a_buf + (ab * kTiles + t) * ly.a_bytes, &map_a, 0, it.a_row[t], 0,
+                      &afull[ab]);
+        }
+        if (PASS == 2) {
+          const int rb = rb_iter & 1;
+          if (!mbar_wait(&rbempty[rb], ((rb_iter >> 1) & 1) ^ 1, abort, p.status)) break;
+          ++rb_iter;
+          mbar_arrive_expect_tx(&rbfull[rb], p.Rp * 4);
+          bulk_load(row_b_all + rb * rbf, p.negb + static_cast<size_t>(it.u) * p.Rp,
+                    p.Rp * 4, &rbfull[rb]);
+        }
+      }
       for (int i = (a_iter > NA ? a_iter - NA : 0); i < a_iter; ++i)
         drain_wait(&afull[i % NA], (i / NA) & 1, p.status);
       for (int i = (rb_iter > 2 ? rb_iter - 2 : 0); i < rb_iter; ++i)
@@ -356,17 +354,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int wg = (warp - 2) >> 2;   // warpgroup = A tile slot of the item
-    const int quarter = warp & 3;     // TMEM lane quarter this warp may access
+    // Warp 2 + 4g + i (g = 0..3): tile slot g & 1, column half g >> 1 of every
+    // accumulator; lane quarter warp % 4 (the TMEM lanes a warp may access).
+    // Four epilogue warps per SM sub-partition hide each other's TMEM-load and
+    // barrier latency.  The two halves of a row (pass 1) or slot (pass 2)
+    // combine at the end of the item: half 1 stores its partial where the
+    // result goes and signals, half 0 reads it back and writes the result.
+    const int grp = (warp - 2) >> 2;
+    const int wg = grp & 1;            // A tile slot of the item
+    const int half = grp >> 1;         // accumulator columns [64 half, 64 half + 64)
+    const int quarter = warp & 3;
     const int lrow = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int tq = wg * 4 + quarter;   // merge barrier pair of this (tile slot, quarter)
     const float c = p.scale_log2;
     int k = 0;        // accumulators of this tile slot consumed
+    int n_merge = 0;  // merges of this (tile slot, quarter): both halves count alike
     int rb_iter = 0;
     bool ok = true;
     for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
       const Item it = decode<PASS>(p, item);
-      const int tile = it.tile[wg];
+      const int tile = wg == 0 ? it.tile[0] : it.tile[1];
       if (PASS == 1) {
         const int r = (tile >= 0 ? tile : 0) * BM + lrow;
         const int qpos = p.T - p.W + (r % p.W);
@@ -383,78 +391,95 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int lo = max(it.pad, c0), hi = min(qpos, c0 + BN - 1);
           const bool fast = __all_sync(0xffffffffu,
                                        row_valid && lo == c0 && hi == c0 + BN - 1);
-          // the whole 128-column accumulator row into registers, then release it
-          uint32_t v[BN / 32][32];
-          float bmx[BN / 32];
+          // this half of the accumulator row into registers, then release it
+          uint32_t v[2][32];
+          float bmx[2] = {-INFINITY, -INFINITY};
+          const uint32_t ta = t_lane + acc * BN + half * 64;
           __syncwarp();
-          const uint32_t ta = t_lane + acc * BN;
           if (fast) {
-#pragma unroll
-            for (int bt = 0; bt < BN / 32; ++bt)
-              tmem_ld32_max(ta + bt * 32, v[bt], bmx[bt]);  // row max from the load path
+            tmem_ld32_max(ta, v[0], bmx[0]);  // block maxima from the load path
+            tmem_ld32_max(ta + 32, v[1], bmx[1]);
           } else {
-#pragma unroll
-            for (int bt = 0; bt < BN / 32; ++bt) tmem_ld32(ta + bt * 32, v[bt]);
+            tmem_ld32(ta, v[0]);
+            tmem_ld32(ta + 32, v[1]);
           }
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&accempty[acc]);
           ++k;
-          if (fast) {
-            const float bm = fmaxf(fmaxf(bmx[0], bmx[1]), fmaxf(bmx[2], bmx[3]));
-            if (bm > mz) {
-              sum *= ex2((mz - bm) * c);
-              mz = bm;
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            // masked columns (padding, not yet seen by the row) drop out by select
+            const int p0 = c0 + (half * 2 + b) * 32;
+            float bm = bmx[b];
+            if (!fast) {
+              bm = -INFINITY;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (p0 + i >= lo && p0 + i <= hi) bm = fmaxf(bm, __uint_as_float(v[b][i]));
+            }
+            // online rescale, only when some row's maximum grew (warp-uniform test)
+            if (__any_sync(0xffffffffu, bm > mz)) {
+              const float sc = bm > mz ? ex2((mz - bm) * c) : 1.f;
+              sum *= sc;
+              mz = fmaxf(mz, bm);
             }
             const float neg = -mz * c;
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            float e[32];
 #pragma unroll
-            for (int bt = 0; bt < BN / 32; ++bt) {
+            for (int i = 0; i < 32; i += 2)
+              fma2(e[i], e[i + 1], __uint_as_float(v[b][i]), __uint_as_float(v[b][i + 1]), c, c,
+                   neg, neg);
 #pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                float x0, x1, x2, x3;
-                fma2(x0, x1, __uint_as_float(v[bt][i]), __uint_as_float(v[bt][i + 1]), c, c,
-                     neg, neg);
-                fma2(x2, x3, __uint_as_float(v[bt][i + 2]), __uint_as_float(v[bt][i + 3]), c,
-                     c, neg, neg);
-                add2(s0, s1, s0, s1, ex2(x0), ex2(x1));
-                add2(s2, s3, s2, s3, ex2(x2), ex2(x3));
-              }
+            for (int i = 0; i < 32; ++i) e[i] = ex2(e[i]);
+            if (!fast) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) e[i] = (p0 + i >= lo && p0 + i <= hi) ? e[i] : 0.f;
             }
-            sum += (s0 + s1) + (s2 + s3);
-          } else if (row_valid) {
 #pragma unroll
-            for (int bt = 0; bt < BN / 32; ++bt) {
-              const int p0 = c0 + bt * 32;
-              float bm = -INFINITY;
+            for (int w = 16; w >= 2; w >>= 1)
 #pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (p0 + i >= lo && p0 + i <= hi) bm = fmaxf(bm, __uint_as_float(v[bt][i]));
-              if (bm > mz) {
-                sum *= ex2((mz - bm) * c);
-                mz = bm;
-              }
-              const float neg = -mz * c;
-              float s0 = 0.f;
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (p0 + i >= lo && p0 + i <= hi)
-                  s0 += ex2(fmaf(__uint_as_float(v[bt][i]), c, neg));
-              sum += s0;
-            }
+              for (int i = 0; i < w; i += 2)
+                add2(e[i], e[i + 1], e[i], e[i + 1], e[i + w], e[i + w + 1]);
+            sum += e[0] + e[1];
           }
         }
         if (!ok) break;
-        if (tile >= 0 && r < p.Rp) {
-          const bool has = row_valid && sum > 0.f;
-          const size_t o = static_cast<size_t>(it.u) * p.Rp + r;
-          p.negb[o] = has ? -(mz * c + log2f(sum)) : -INFINITY;
-          p.pmax[o] = has ? 1.0f / sum : 0.f;
+        if (tile < 0) continue;
+        const size_t o = static_cast<size_t>(it.u) * p.Rp + r;
+        const bool in_rows = r < p.Rp;
+        if (half == 1) {
+          // partial (max, sum) of columns [64, 128) of every chunk
+          if (!epi_wait(&mrg_empty[tq], (n_merge & 1) ^ 1, abort, p.status, lane)) break;
+          if (in_rows) {
+            p.negb[o] = mz;
+            p.pmax[o] = sum;
+          }
+          __threadfence_block();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mrg_full[tq]);
+        } else {
+          if (!epi_wait(&mrg_full[tq], n_merge & 1, abort, p.status, lane)) break;
+          __syncwarp();
+          const float m2 = in_rows ? __ldcg(p.negb + o) : -INFINITY;
+          const float s2 = in_rows ? __ldcg(p.pmax + o) : 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mrg_empty[tq]);
+          const float M = fmaxf(mz, m2);
+          const float S = (M == -INFINITY)
+                              ? 0.f
+                              : sum * ex2((mz - M) * c) + s2 * ex2((m2 - M) * c);
+          if (in_rows) {
+            const bool has = row_valid && S > 0.f;
+            p.negb[o] = has ? -(M * c + log2f(S)) : -INFINITY;
+            p.pmax[o] = has ? 1.0f / S : 0.f;
+          }
         }
+        ++n_merge;
       } else {
         if (it.n_ch == 0) continue;
-        // the unit's negated row constants (bulk copy by the TMA warp)
+        // the unit's negated row constants (bulk copy by the loader warp)
         const int rb = rb_iter & 1;
         if (!epi_wait(&rbfull[rb], (rb_iter >> 1) & 1, abort, p.status, lane)) break;
         ++rb_iter;
@@ -471,49 +496,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t v[BN / 32][32];
+          uint32_t v[2][32];
+          const uint32_t ta = t_lane + acc * BN + half * 64;
           __syncwarp();
-          const uint32_t ta = t_lane + acc * BN;
-#pragma unroll
-          for (int bt = 0; bt < BN / 32; ++bt) tmem_ld32(ta + bt * 32, v[bt]);
+          tmem_ld32(ta, v[0]);
+          tmem_ld32(ta + 32, v[1]);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&accempty[acc]);
           ++k;
 #pragma unroll
-          for (int bt = 0; bt < BN / 32; ++bt) {
-            const float* rbb = row_b + ch * BN + bt * 32;
-            if (fast) {
+          for (int b = 0; b < 2; ++b) {
+            const int r0 = ch * BN + (half * 2 + b) * 32;  // first query row of the block
+            const float* rbb = row_b + r0;
+            float e[32];
 #pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                const float4 nb = lds128(rbb + i);  // negated row constants
-                float x0, x1, x2, x3;
-                fma2(x0, x1, __uint_as_float(v[bt][i]), __uint_as_float(v[bt][i + 1]), c, c,
-                     nb.x, nb.y);
-                fma2(x2, x3, __uint_as_float(v[bt][i + 2]), __uint_as_float(v[bt][i + 3]), c,
-                     c, nb.z, nb.w);
-                add2(a0, a1, a0, a1, ex2(x0), ex2(x1));
-                add2(a2, a3, a2, a3, ex2(x2), ex2(x3));
-              }
-            } else if (pos_valid) {
-              const int r0 = ch * BN + bt * 32;
+            for (int i = 0; i < 32; i += 4) {
+              const float4 nb = lds128(rbb + i);  // negated row constants (-inf past R)
+              fma2(e[i], e[i + 1], __uint_as_float(v[b][i]), __uint_as_float(v[b][i + 1]), c, c,
+                   nb.x, nb.y);
+              fma2(e[i + 2], e[i + 3], __uint_as_float(v[b][i + 2]),
+                   __uint_as_float(v[b][i + 3]), c, c, nb.z, nb.w);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) e[i] = ex2(e[i]);
+            if (!fast) {
+              // window query j sees this slot only if j >= jmin
               int j = r0 % p.W;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                if (j >= jmin && r0 + i < p.R)
-                  a0 += ex2(fmaf(__uint_as_float(v[bt][i]), c, lds32(rbb + i)));
+                e[i] = j >= jmin ? e[i] : 0.f;
                 j = (j + 1 == p.W) ? 0 : j + 1;
               }
             }
+#pragma unroll
+            for (int w = 16; w >= 4; w >>= 1)
+#pragma unroll
+              for (int i = 0; i < w; i += 2)
+                add2(e[i], e[i + 1], e[i], e[i + 1], e[i + w], e[i + w + 1]);
+            add2(a0, a1, a0, a1, e[0], e[1]);
+            add2(a2, a3, a2, a3, e[2], e[3]);
           }
         }
         // every epilogue warp releases the row constants, tile or no tile
         __syncwarp();
         if (lane == 0) mbar_arrive(&rbempty[rb]);
         if (!ok) break;
-        if (pos_valid)
-          p.usage[static_cast<size_t>(it.u) * p.T + pos] = (a0 + a1) + (a2 + a3);
+        if (tile < 0) continue;
+        const float part = (a0 + a1) + (a2 + a3);
+        float* dst = p.usage + static_cast<size_t>(it.u) * p.T + pos;
+        if (half == 1) {
+          // partial usage over the query rows of columns [64, 128) of every chunk
+          if (!epi_wait(&mrg_empty[tq], (n_merge & 1) ^ 1, abort, p.status, lane)) break;
+          if (pos_valid) *dst = part;
+          __threadfence_block();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mrg_full[tq]);
+        } else {
+          if (!epi_wait(&mrg_full[tq], n_merge & 1, abort, p.status, lane)) break;
+          __syncwarp();
+          const float other = pos_valid ? __ldcg(dst) : 0.f;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&mrg_empty[tq]);
+          if (pos_valid) *dst = part + other;
+        }
+        ++n_merge;
       }
     }
   }
