@@ -30,6 +30,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxK = 1024;  // thresholds: delta >= 1/1024
+constexpr int kFastSegs = 256;  // segment count up to which the quota correction ranks directly
 
 __device__ __forceinline__ uint64_t fixed_mass(float m) {
   // m * 2^40 is exact in fp32 (an exponent shift); truncation toward zero.
@@ -75,12 +76,74 @@ __device__ __forceinline__ int64_t bids_ge(int64_t b0, int64_t M, int64_t cap, i
 }
 
 __device__ void take_best_bids(const int64_t* rem, const int32_t* ref, int32_t* q, int ns,
-                               int64_t M, int64_t D,
-                               bool negate, bool low_first, int lane) {
+                               int64_t M, int64_t D, bool negate, bool low_first, int lane,
+                               int32_t* scratch) {
   auto b0_of = [&](int s) { return negate ? -rem[s] : rem[s]; };
   auto cap_of = [&](int s) -> int64_t {
     return negate ? static_cast<int64_t>(q[s]) - ref[s] : static_cast<int64_t>(ref[s]) - q[s];
   };
+  // Fast exact path.  Round-half-up leaves every first bid of a segment with
+  // spare capacity in (-M/2, M/2] (short) or [-M/2, M/2) (over), so bids of
+  // round r (k = r) all lie below every bid of round r-1: the D best bids are
+  // whole rounds (one unit to every segment with capacity left) plus the D'
+  // best first bids of the next round, in (bid, index) order.  No division.
+  bool in_range = ns <= kFastSegs;
+  for (int s = lane; s < ns; s += 32) {
+    if (cap_of(s) <= 0) continue;
+    const int64_t twice = 2 * b0_of(s);
+    in_range = in_range && (negate ? (twice >= -M && twice < M) : (twice > -M && twice <= M));
+  }
+  if (__all_sync(0xffffffffu, in_range)) {
+    // complete rounds r: the largest r with sum_s min(cap_s, r) <= D
+    auto given = [&](int64_t r) {
+      int64_t g = 0;
+      for (int s = lane; s < ns; s += 32) {
+        const int64_t cap = cap_of(s);
+        g += cap <= 0 ? 0 : (cap < r ? cap : r);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+      return g;
+    };
+    int64_t rmax = 0;
+    for (int s = lane; s < ns; s += 32) {
+      const int64_t cap = cap_of(s);
+      rmax = cap > rmax ? cap : rmax;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const int64_t t = __shfl_xor_sync(0xffffffffu, rmax, o);
+      rmax = t > rmax ? t : rmax;
+    }
+    int64_t r = 0, r_hi = rmax;  // given(0) = 0 <= D
+    while (r < r_hi) {
+      const int64_t mid = r + (r_hi - r + 1) / 2;
+      if (given(mid) <= D) r = mid; else r_hi = mid - 1;
+    }
+    D -= given(r);
+    // round r: the D best first bids among the segments with capacity > r
+    for (int s = lane; s < ns; s += 32) {
+      const int64_t cap = cap_of(s);
+      int64_t t = cap < r ? cap : r;
+      if (cap > r && D > 0) {
+        const int64_t b0 = b0_of(s);
+        int64_t rank = 0;
+        for (int j = 0; j < ns; ++j) {
+          if (j == s || cap_of(j) <= r) continue;
+          const int64_t bj = b0_of(j);
+          rank += (bj > b0 || (bj == b0 && (low_first ? j < s : j > s))) ? 1 : 0;
+        }
+        if (rank < D) t += 1;
+      }
+      scratch[s] = static_cast<int32_t>(t);
+    }
+    __syncwarp();
+    for (int s = lane; s < ns; s += 32) q[s] = negate ? q[s] - scratch[s] : q[s] + scratch[s];
+    __syncwarp();
+    return;
+  }
+  // General path (bids outside that range cannot arise from the rounding rule;
+  // kept so that the routine is exact for any input).
   // search range: every bid lies in [lo, hi]
   int64_t lo = INT64_MAX, hi = INT64_MIN;
   for (int s = lane; s < ns; s += 32) {
@@ -152,6 +215,7 @@ __global__ void __launch_bounds__(kThreads)
   int32_t* s_q = s_len + p.S_cap;
   int32_t* s_floor = s_q + p.S_cap;
   __shared__ int32_t s_b[kMaxK];
+  __shared__ uint64_t s_tau[kMaxK];
   __shared__ uint64_t s_warp[kThreads / 32];
   __shared__ uint64_t s_total;
   __shared__ int s_nseg;
@@ -199,19 +263,25 @@ __global__ void __launch_bounds__(kThreads)
   const uint64_t before = s_warp[warp] + incl - local;  // prefix before `lo`
   const uint64_t S = s_total;
 
-  // ---- 2. cut points: b_k = min{t in [1,n] : C(t) >= tau_k}
+  // ---- 2. cut points: b_k = min{t in [1,n] : C(t) >= tau_k}; each threshold
+  // is computed once (fp64 is slow on this part), then found by the thread
+  // whose range holds it
   const double S_d = __ull2double_rn(S);
-  for (int k = 1; k <= p.K; ++k) {
-    const double frac = __dmul_rn(static_cast<double>(k), p.delta);
-    const uint64_t tau = static_cast<uint64_t>(ceil(__dmul_rn(frac, S_d)));
+  for (int k = threadIdx.x; k < p.K; k += kThreads) {
+    const double frac = __dmul_rn(static_cast<double>(k + 1), p.delta);
+    s_tau[k] = static_cast<uint64_t>(ceil(__dmul_rn(frac, S_d)));
+  }
+  __syncthreads();
+  for (int k = 0; k < p.K; ++k) {
+    const uint64_t tau = s_tau[k];
     if (tau == 0) {
-      if (threadIdx.x == 0) s_b[k - 1] = 1;
+      if (threadIdx.x == 0) s_b[k] = 1;
     } else if (before < tau && tau <= before + local) {
       uint64_t c = before;
       for (int v = lo; v < hi; ++v) {
         c += fixed_mass(m[v]);
         if (c >= tau) {
-          s_b[k - 1] = v + 1;
+          s_b[k] = v + 1;
           break;
         }
       }
@@ -354,12 +424,14 @@ __global__ void __launch_bounds__(kThreads)
       // segment s bids rem_s - k*Mt for k < L_s - q_s; take the D largest,
       // ties between segments -> lower index first.
       take_best_bids(s_rem, s_len, s_q, ns, static_cast<int64_t>(Mt),
-                     budget - qtot, /*negate=*/false, /*low_first=*/true, lane);
+                     budget - qtot, /*negate=*/false, /*low_first=*/true, lane,
+                     reinterpret_cast<int32_t*>(s_mass));
     } else if (qtot > budget) {
       // segment s bids rem_s + k*Mt for k < q_s - floor_s; take the D smallest,
       // ties -> higher index first (the negated bids, largest first).
       take_best_bids(s_rem, s_floor, s_q, ns, static_cast<int64_t>(Mt),
-                     qtot - budget, /*negate=*/true, /*low_first=*/false, lane);
+                     qtot - budget, /*negate=*/true, /*low_first=*/false, lane,
+                     reinterpret_cast<int32_t*>(s_mass));
     }
   }
   __syncthreads();

@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kRegPer = 8;  // slots per thread up to which the excess search keeps keys in registers
 
 enum : uint8_t { kOut = 0, kMust = 1, kPick = 2 };
 
@@ -88,6 +89,44 @@ __device__ __forceinline__ void pick_segment(const float* sc, uint8_t* flag, int
   }
 }
 
+// As pick_segment for segments of at most 32*PER slots, with the candidates'
+// keys held in registers across the search.
+template <int PER>
+__device__ __forceinline__ void pick_segment_reg(const float* sc, uint8_t* flag, int st, int en,
+                                                 int want, int lane) {
+  uint32_t key[PER];
+  bool cand[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int v = st + lane + 32 * i;
+    cand[i] = v < en && flag[v] == kOut;
+    key[i] = cand[i] ? score_key(sc, v) : 0u;
+  }
+  uint32_t x = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t t = x | (1u << bit);
+    unsigned cnt = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) cnt += (cand[i] && key[i] >= t) ? 1u : 0u;
+    if (static_cast<int>(__reduce_add_sync(0xffffffffu, cnt)) >= want) x = t;
+  }
+  unsigned gt = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) gt += (cand[i] && key[i] > x) ? 1u : 0u;
+  int ties_left = want - static_cast<int>(__reduce_add_sync(0xffffffffu, gt));
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {  // 32-slot groups in slot order
+    const bool tie = cand[i] && key[i] == x;
+    const uint32_t ball = __ballot_sync(0xffffffffu, tie);
+    const bool take = (cand[i] && key[i] > x) ||
+                      (tie && static_cast<int>(__popc(ball & below)) < ties_left);
+    ties_left -= __popc(ball);
+    if (take) flag[st + lane + 32 * i] = kPick;
+  }
+  __syncwarp();
+}
+
 __global__ void __launch_bounds__(kThreads)
     select_kernel(SelParams p) {
   extern __shared__ uint8_t sm[];
@@ -95,6 +134,7 @@ __global__ void __launch_bounds__(kThreads)
   int32_t* s_want = s_start + p.S_max;                            // [S_max]
   uint8_t* flag = reinterpret_cast<uint8_t*>(s_want + p.S_max);  // [T]
   __shared__ int red[kWarps];
+  __shared__ int red2[2 * kWarps];
   __shared__ int s_scan[kWarps];
 
   const int u = blockIdx.x;
@@ -132,7 +172,11 @@ __global__ void __launch_bounds__(kThreads)
     const int st = s_start[s];
     const int en = (s + 1 < ns) ? max(st, s_start[s + 1]) : n;
     const int want = s_want[s];
-    if (want > 0) pick_segment(sc, flag, st, en, want, lane);
+    if (want <= 0) continue;
+    if (en - st <= 32 * 8)
+      pick_segment_reg<8>(sc, flag, st, en, want, lane);
+    else
+      pick_segment(sc, flag, st, en, want, lane);
   }
   __syncthreads();
 
@@ -144,11 +188,37 @@ __global__ void __launch_bounds__(kThreads)
   if (excess > 0) {
     // x = the excess-th smallest pick key: largest x with #(pick key < x) < excess
     uint32_t x = 0;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t t = x | (1u << bit);
-      int cnt = 0;
-      for (int v = lo; v < hi; ++v) cnt += (flag[v] == kPick && score_key(sc, v) < t) ? 1 : 0;
-      if (block_count(cnt, red) < excess) x = t;
+    if (per <= kRegPer) {  // CTA-uniform: every thread takes the same branch (barriers inside)
+      uint32_t key[kRegPer];
+      bool pk[kRegPer];
+#pragma unroll
+      for (int i = 0; i < kRegPer; ++i) {
+        const int v = lo + i;
+        pk[i] = v < hi && flag[v] == kPick;
+        key[i] = pk[i] ? score_key(sc, v) : 0u;
+      }
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t t = x | (1u << bit);
+        unsigned cnt = 0;
+#pragma unroll
+        for (int i = 0; i < kRegPer; ++i) cnt += (pk[i] && key[i] < t) ? 1u : 0u;
+        cnt = __reduce_add_sync(0xffffffffu, cnt);
+        // alternate buffers: one barrier per step
+        int* rb = red2 + (bit & 1) * kWarps;
+        if (lane == 0) rb[warp] = static_cast<int>(cnt);
+        __syncthreads();
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) total += rb[w];
+        if (total < excess) x = t;
+      }
+    } else {
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t t = x | (1u << bit);
+        int cnt = 0;
+        for (int v = lo; v < hi; ++v) cnt += (flag[v] == kPick && score_key(sc, v) < t) ? 1 : 0;
+        if (block_count(cnt, red) < excess) x = t;
+      }
     }
     int lt = 0, ties = 0;
     for (int v = lo; v < hi; ++v) {
