@@ -12,24 +12,27 @@
 // Each softmax row needs its normaliser before its probabilities can be summed
 // per slot, and the normaliser spans every slot.  The work is therefore split
 // into two tensor-core passes over the same QK^T:
-//   pass 1: rows on TMEM lanes (A = query rows, B = 128-slot chunks of K);
+//   pass 1: rows on TMEM lanes (A = query rows, B = 256-slot chunks of K);
 //           each epilogue thread owns one row and keeps an online max / sum;
 //           out: -b_r (b_r = log2 of the row normaliser in the scaled log2
 //           domain) and 1/Z'_r (the row's largest probability).
-//   pass 2: slots on TMEM lanes (A = cached keys, B = 128-row chunks of Q);
+//   pass 2: slots on TMEM lanes (A = cached keys, B = 256-row chunks of Q);
 //           each epilogue thread owns one slot and sums
 //           exp2(scale*log2e*z - b_r) over the rows.
-// Work item = one unit and a PAIR of 128-row A tiles: every B chunk that TMA
-// brings in feeds two MMAs (one per tile), which halves the operand traffic
-// per FLOP.  Persistent warp-specialised CTAs: warp 0 streams B chunks
-// through a ring (TMA), warp 18 loads the A tiles (double-buffered across
-// items) and, in pass 2, the item's row constants (one bulk copy), warp 1
-// issues tcgen05.mma into four TMEM accumulators (tile x parity), and 16
-// epilogue warps (warps 2-17: tile slot x column half x lane quarter) drain
-// them: each copies its 32 rows x 64 columns of an accumulator to registers,
-// hands the accumulator back, then computes; the two column halves of a row
-// (pass 1) or slot (pass 2) are combined at the end of the item.  Every wait
-// is bounded.
+// Work item = one unit and a PAIR of 128-row A tiles: every 256-row B chunk
+// that TMA brings in feeds one M128 x N256 MMA group per tile, which halves
+// the operand traffic per FLOP.  Each tile has one 256-column TMEM
+// accumulator; the two tiles alternate, so one tile's accumulator drains
+// while the other's MMAs run.
+//
+// Persistent warp-specialised CTAs: warp 0 streams B chunks through a ring
+// (TMA), warp 18 loads each tile slot's A tile (reloaded as soon as the slot's
+// last MMA of an item completes) and, in pass 2, the item's row constants (one
+// bulk copy), warp 1 issues tcgen05.mma, and 16 epilogue warps (warps 2-17:
+// tile slot x column half x lane quarter) drain the accumulators, 64 columns
+// at a time, releasing an accumulator once its last columns are in registers.
+// The two column halves of a row (pass 1) or slot (pass 2) are combined at
+// the end of the item.  Every wait is bounded.
 #include <cmath>
 #include <cstdio>
 
@@ -38,19 +41,20 @@
 namespace kvc {
 namespace {
 
-constexpr int kEpiWarps = 16;                       // tile slot x column half x lane quarter
-constexpr int kLoaderWarp = 2 + kEpiWarps;          // A tiles / row constants
-constexpr int kThreads = 32 * (kLoaderWarp + 1);    // B warp, MMA warp, epilogue, loader
-constexpr int BM = 128;        // A-operand rows per tile (TMEM lanes)
-constexpr int BN = 128;        // B-operand rows per chunk (TMEM columns)
-constexpr int kTiles = 2;      // A tiles per work item
-constexpr int kMaxStages = 6;  // B ring depth limit
-constexpr int kAccCols = 2 * kTiles * BN;  // accumulators: tile x parity = 512 columns
-constexpr int kBarriers = 48;              // mbarrier slots in shared memory
+constexpr int kEpiWarps = 16;                     // tile slot x column half x lane quarter
+constexpr int kLoaderWarp = 2 + kEpiWarps;        // A tiles / row constants
+constexpr int kThreads = 32 * (kLoaderWarp + 1);  // B warp, MMA warp, epilogue, loader
+constexpr int BM = 128;         // A-operand rows per tile (TMEM lanes)
+constexpr int BN = 256;         // B-operand rows per chunk (accumulator columns)
+constexpr int kHalf = BN / 2;   // accumulator columns per epilogue column half
+constexpr int kTiles = 2;       // A tiles per work item
+constexpr int kMaxStages = 6;   // B ring depth limit
+constexpr int kAccCols = kTiles * BN;  // one accumulator per tile slot: 512 columns
+constexpr int kBarriers = 48;          // mbarrier slots in shared memory
 
 struct Params {
   int U, T, R, Rp, W, B, H;
-  int n_items, n_tiles, n_pairs, n_stages, n_abuf, unit_major;
+  int n_items, n_tiles, n_pairs, n_stages, unit_major;
   float scale_log2;
   const int32_t* pad;
   float* negb;    // [U][Rp] -b_r (pass 1 writes, pass 2 reads by bulk copy)
@@ -60,11 +64,10 @@ struct Params {
 };
 
 struct Item {
-  int u, pad, n_ch, c_start;
+  int u, pad, n_ch, c_start, c_end;  // chunks cover [c_start, c_end) of the B rows
   int tile[kTiles];   // tile index within the unit, -1 if absent
   int a_row[kTiles];  // first A row of the tile in the 2-D tensor view
   int b_row0;         // first B row of chunk 0
-  int n_present;
 };
 
 template <int PASS>
@@ -74,7 +77,7 @@ __device__ __forceinline__ Item decode(const Params& p, int item) {
   const int pair = item - it.u * p.n_pairs;
   const int b = (it.u / p.H) % p.B;
   it.pad = min(max(p.pad[b], 0), p.T);
-  it.n_present = 0;
+  int n_present = 0;
 #pragma unroll
   for (int t = 0; t < kTiles; ++t) {
     const int tile = pair * kTiles + t;
@@ -82,29 +85,36 @@ __device__ __forceinline__ Item decode(const Params& p, int item) {
     if (PASS == 2) present = present && (tile * BM + BM > it.pad);  // not all padding
     it.tile[t] = present ? tile : -1;
     it.a_row[t] = (PASS == 1) ? it.u * p.R + tile * BM : it.u * p.T + tile * BM;
-    it.n_present += present ? 1 : 0;
+    n_present += present ? 1 : 0;
   }
   if (PASS == 1) {
     it.c_start = (it.pad / BN) * BN;
-    it.n_ch = (it.pad < p.T && it.n_present) ? (p.T - it.c_start + BN - 1) / BN : 0;
+    it.c_end = p.T;
     it.b_row0 = it.u * p.T + it.c_start;
   } else {
     it.c_start = 0;
-    it.n_ch = (it.pad < p.T && it.n_present) ? (p.R + BN - 1) / BN : 0;
+    it.c_end = p.R;
     it.b_row0 = it.u * p.R;
   }
+  it.n_ch = (it.pad < p.T && n_present) ? (it.c_end - it.c_start + BN - 1) / BN : 0;
   return it;
+}
+
+// Accumulator columns (= MMA N) of chunk ch: the rows left, rounded up to the
+// 32-column block of the epilogue (a multiple of 16, as the MMA needs).
+__device__ __forceinline__ int chunk_cols(const Item& it, int ch) {
+  const int left = it.c_end - (it.c_start + ch * BN);
+  return left >= BN ? BN : ((left + 31) & ~31);
 }
 
 // Shared-memory layout (byte offsets from the 1024-aligned base).
 struct Layout {
-  int a_bytes, b_bytes, kb;  // per tile / per stage, 64-element K blocks
+  int a_bytes, b_bytes;  // per tile / per stage
   int off_b, off_bars, off_misc, off_rowb, total;
-  __host__ __device__ Layout(int D, int n_stages, int rowb_floats, int n_abuf) {
-    kb = D / 64;
+  __host__ __device__ Layout(int D, int n_stages, int rowb_floats) {
     a_bytes = BM * D * 2;
     b_bytes = BN * D * 2;
-    off_b = n_abuf * kTiles * a_bytes;  // A: [n_abuf items][2 tiles]
+    off_b = kTiles * a_bytes;  // A: one buffer per tile slot
     off_bars = off_b + n_stages * b_bytes;
     off_misc = off_bars + kBarriers * 8;
     off_rowb = off_misc + 16;
@@ -165,14 +175,128 @@ __device__ __forceinline__ int cta_item(const Params& p, int k) {
   return item < p.n_items ? item : -1;
 }
 
+// Pass-1 row statistics of one 32-column block: online max (rescaling the
+// running sum when it grows) and the sum of exp2(c*z - c*max) over the block's
+// valid columns [lo, hi] (all of them when FULL; the masked form is a separate
+// instantiation so that its selects never run on full blocks).
+template <bool FULL>
+__device__ __forceinline__ void row_block(const uint32_t (&v)[32], float bmx, int p0, int lo,
+                                          int hi, float c, float& mz, float& sum) {
+  // valid columns of the block as a bit mask (bit i = column p0 + i)
+  uint32_t valid = 0xffffffffu;
+  if constexpr (!FULL) {
+    const int a = max(lo - p0, 0), b = min(hi - p0, 31);
+    valid = (b < a) ? 0u : ((0xffffffffu >> (31 - b)) & (0xffffffffu << a));
+  }
+  float bm = bmx;
+  if constexpr (!FULL) {
+    bm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      bm = (valid & (1u << i)) ? fmaxf(bm, __uint_as_float(v[i])) : bm;
+  }
+  // rescale only when some row's maximum grew (warp-uniform test)
+  if (__any_sync(0xffffffffu, bm > mz)) {
+    const float sc = bm > mz ? ex2((mz - bm) * c) : 1.f;
+    sum *= sc;
+    mz = fmaxf(mz, bm);
+  }
+  const float neg = -mz * c;
+  const float2 cc = make_float2(c, c), nn = make_float2(neg, neg);
+  float2 e[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    e[i] = fma2(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), cc, nn);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    e[i].x = ex2(e[i].x);
+    e[i].y = ex2(e[i].y);
+  }
+  if constexpr (!FULL) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      e[i].x = (valid & (1u << (2 * i))) ? e[i].x : 0.f;
+      e[i].y = (valid & (2u << (2 * i))) ? e[i].y : 0.f;
+    }
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) e[i] = add2(e[i], e[i + w]);
+  sum += e[0].x + e[0].y;
+}
+
+// Pass-2 slot usage of one 32-row block (query rows r0 .. r0+31): sum of
+// exp2(c*z - b_r) with the negated row constants from shared memory; rows of
+// window index j < jmin do not see the slot (dropped unless FULL).
+template <bool FULL>
+__device__ __forceinline__ void slot_block(const uint32_t (&v)[32], const float* rbb, int r0,
+                                           int W, int jmin, float c,
+                                           float2& acc) {
+  const float2 cc = make_float2(c, c);
+  float2 e[16];
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float4 nb = lds128(rbb + 2 * i);  // negated row constants (-inf past R)
+    e[i] = fma2(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), cc,
+                make_float2(nb.x, nb.y));
+    e[i + 1] = fma2(make_float2(__uint_as_float(v[2 * i + 2]), __uint_as_float(v[2 * i + 3])),
+                    cc, make_float2(nb.z, nb.w));
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    e[i].x = ex2(e[i].x);
+    e[i].y = ex2(e[i].y);
+  }
+  if constexpr (!FULL) {
+    const int j0 = r0 % W;
+    if (W % 32 == 0) {
+      // the block's rows are window indices j0 .. j0+31 (no wrap)
+      const int first = jmin - j0;  // rows i >= first see the slot
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        e[i].x = 2 * i >= first ? e[i].x : 0.f;
+        e[i].y = 2 * i + 1 >= first ? e[i].y : 0.f;
+      }
+    } else {
+      int j = j0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        e[i].x = j >= jmin ? e[i].x : 0.f;
+        j = (j + 1 == W) ? 0 : j + 1;
+        e[i].y = j >= jmin ? e[i].y : 0.f;
+        j = (j + 1 == W) ? 0 : j + 1;
+      }
+    }
+  }
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) e[i] = add2(e[i], e[i + w]);
+  acc = add2(acc, e[0]);
+}
+
+// Copy two 32-column blocks of this warp's accumulator rows to registers,
+// with the per-block maxima from the load path when `with_max` (warp-uniform).
+__device__ __forceinline__ void load2(uint32_t taddr, bool with_max, uint32_t (&v)[2][32],
+                                      float (&bmx)[2]) {
+  if (with_max) {
+    tmem_ld32_max(taddr, v[0], bmx[0]);
+    tmem_ld32_max(taddr + 32, v[1], bmx[1]);
+  } else {
+    tmem_ld32(taddr, v[0]);
+    tmem_ld32(taddr + 32, v[1]);
+    bmx[0] = bmx[1] = -INFINITY;
+  }
+}
+
 template <int D, int PASS>
 __global__ void __launch_bounds__(kThreads, 1)
     usage_kernel(const __grid_constant__ CUtensorMap map_a,
                  const __grid_constant__ CUtensorMap map_b, Params p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
   const int rbf = (PASS == 2) ? rowb_floats(p.R) : 0;
-  const Layout ly(D, p.n_stages, rbf, p.n_abuf);
-  const int NA = p.n_abuf;
+  const Layout ly(D, p.n_stages, rbf);
   const int NS = p.n_stages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle, as an offset from the shared
@@ -182,18 +306,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* a_buf = smem;
   uint8_t* b_buf = smem + ly.off_b;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + ly.off_bars);
-  uint64_t* full = bars;                          // [kMaxStages]
-  uint64_t* empty = bars + kMaxStages;            // [kMaxStages]
-  uint64_t* afull = bars + 2 * kMaxStages;        // [2]
-  uint64_t* aempty = afull + 2;                   // [2]
-  uint64_t* accfull = aempty + 2;                 // [4]  tile * 2 + parity
-  uint64_t* accempty = accfull + 4;               // [4]  (one arrival per epilogue warp of the tile)
-  uint64_t* done = accempty + 4;                  // [1]
-  uint64_t* rbfull = done + 1;                    // [2]  pass 2 row constants landed
-  uint64_t* rbempty = rbfull + 2;                 // [2]  pass 2 row constants consumed (all epilogue warps)
-  uint64_t* mrg_full = rbempty + 2;               // [8]  half 1's partials stored (tile slot x quarter)
-  uint64_t* mrg_empty = mrg_full + 2 * 4;         // [8]  half 0 has read them
-  static_assert(2 * kMaxStages + 2 + 2 + 4 + 4 + 1 + 2 + 2 + 8 + 8 <= kBarriers,
+  uint64_t* full = bars;                      // [kMaxStages] B stage landed
+  uint64_t* empty = bars + kMaxStages;        // [kMaxStages] B stage consumed
+  uint64_t* afull = bars + 2 * kMaxStages;    // [kTiles] tile slot's A landed
+  uint64_t* aempty = afull + kTiles;          // [kTiles] tile slot's A consumed
+  uint64_t* accfull = aempty + kTiles;        // [kTiles] tile slot's accumulator written
+  uint64_t* accempty = accfull + kTiles;      // [kTiles] ... drained (its 8 epilogue warps)
+  uint64_t* done = accempty + kTiles;         // [1]
+  uint64_t* rbfull = done + 1;                // [2] pass 2 row constants landed
+  uint64_t* rbempty = rbfull + 2;             // [2] ... consumed (all epilogue warps)
+  uint64_t* mrg_full = rbempty + 2;           // [8] half 1's partials stored (slot x quarter)
+  uint64_t* mrg_empty = mrg_full + 2 * 4;     // [8] half 0 has read them
+  static_assert(2 * kMaxStages + 4 * kTiles + 1 + 2 + 2 + 8 + 8 <= kBarriers,
                 "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ly.off_misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + ly.off_misc + 4);
@@ -205,15 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&afull[t], 1);
+      mbar_init(&aempty[t], 1);
+      mbar_init(&accfull[t], 1);
+      mbar_init(&accempty[t], 8);  // 4 lane quarters x 2 column halves
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&afull[b], 1);
-      mbar_init(&aempty[b], 1);
       mbar_init(&rbfull[b], 1);
       mbar_init(&rbempty[b], kEpiWarps);
-    }
-    for (int a = 0; a < 4; ++a) {
-      mbar_init(&accfull[a], 1);
-      mbar_init(&accempty[a], 8);  // 4 lane quarters x 2 column halves
     }
     for (int m = 0; m < 8; ++m) {
       mbar_init(&mrg_full[m], 1);
@@ -263,27 +387,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kLoaderWarp) {
     // ------------------------------------------- A tiles and row constants
-    // Runs up to two items ahead of the MMA warp, independently of the B ring,
-    // so that an item's A tiles (and in pass 2 its row constants) have landed
-    // by the time its first B chunk arrives.
+    // A tile slot t is reloaded as soon as the slot's last MMA of the previous
+    // item has completed, while the other slot's MMAs still run.
     if (lane == 0) {
-      int a_iter = 0, rb_iter = 0;
+      int a_cnt[kTiles] = {0, 0};
+      int rb_iter = 0;
       bool ok = true;
       for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
         if (it.n_ch == 0) continue;
-        const int ab = a_iter % NA;
-        if (!mbar_wait(&aempty[ab], ((a_iter / NA) & 1) ^ 1, abort, p.status)) break;
-        ++a_iter;
-        mbar_arrive_expect_tx(&afull[ab], it.n_present * ly.a_bytes);
 #pragma unroll
         for (int t = 0; t < kTiles; ++t) {
-          if (it.tile[t] < 0) continue;
+          if (!ok || it.tile[t] < 0) continue;
+          if (!mbar_wait(&aempty[t], (a_cnt[t] & 1) ^ 1, abort, p.status)) {
+            ok = false;
+            continue;
+          }
+          ++a_cnt[t];
+          mbar_arrive_expect_tx(&afull[t], ly.a_bytes);
           // one box: 128 rows x all 64-element K blocks, K block outermost
-          tma_load_3d(a_buf + (ab * kTiles + t) * ly.a_bytes, &map_a, 0, it.a_row[t], 0,
-                      &afull[ab]);
+          tma_load_3d(a_buf + t * ly.a_bytes, &map_a, 0, it.a_row[t], 0, &afull[t]);
         }
-        if (PASS == 2) {
+        if (ok && PASS == 2) {
           const int rb = rb_iter & 1;
           if (!mbar_wait(&rbempty[rb], ((rb_iter >> 1) & 1) ^ 1, abort, p.status)) break;
           ++rb_iter;
@@ -292,8 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     p.Rp * 4, &rbfull[rb]);
         }
       }
-      for (int i = (a_iter > NA ? a_iter - NA : 0); i < a_iter; ++i)
-        drain_wait(&afull[i % NA], (i / NA) & 1, p.status);
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t)
+        if (a_cnt[t] > 0) drain_wait(&afull[t], (a_cnt[t] - 1) & 1, p.status);
       for (int i = (rb_iter > 2 ? rb_iter - 2 : 0); i < rb_iter; ++i)
         drain_wait(&rbfull[i & 1], (i >> 1) & 1, p.status);
     }
@@ -301,52 +427,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN);
       const uint32_t a_base = smem_u32(a_buf), b_base = smem_u32(b_buf);
-      int a_iter = 0, b_iter = 0;
-      int kt[kTiles] = {0, 0};  // accumulators filled per tile
+      int a_cnt[kTiles] = {0, 0};  // A loads consumed per tile slot
+      int kt[kTiles] = {0, 0};     // accumulator fills per tile slot
+      int b_iter = 0;
       bool ok = true;
       for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
-        if (it.n_ch == 0) continue;
-        const int ab = a_iter % NA;
-        if (!mbar_wait(&afull[ab], (a_iter / NA) & 1, abort, p.status)) {
-          ok = false;
-          break;
-        }
-        ++a_iter;
         for (int c = 0; ok && c < it.n_ch; ++c) {
           const int s = b_iter % NS;
           if (!mbar_wait(&full[s], (b_iter / NS) & 1, abort, p.status)) {
             ok = false;
             break;
           }
+          const uint32_t idesc = idesc_bf16_f32(BM, chunk_cols(it, c));
           const uint32_t b_tile = b_base + s * ly.b_bytes;
 #pragma unroll
           for (int t = 0; t < kTiles; ++t) {
-            if (it.tile[t] < 0) continue;
-            const int acc = t * 2 + (kt[t] & 1);
-            if (!mbar_wait(&accempty[acc], ((kt[t] >> 1) & 1) ^ 1, abort, p.status)) {
+            if (!ok || it.tile[t] < 0) continue;
+            if (c == 0) {
+              if (!mbar_wait(&afull[t], a_cnt[t] & 1, abort, p.status)) {
+                ok = false;
+                continue;
+              }
+              ++a_cnt[t];
+            }
+            if (!mbar_wait(&accempty[t], (kt[t] & 1) ^ 1, abort, p.status)) {
               ok = false;
-              break;
+              continue;
             }
             tc_fence_after();
-            const uint32_t a_tile = a_base + (ab * kTiles + t) * ly.a_bytes;
+            const uint32_t a_tile = a_base + t * ly.a_bytes;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
-              const int kb = k / 4, kk = k % 4;
-              const uint64_t ad = sw128_desc(a_tile + kb * BM * 128 + kk * 32);
-              const uint64_t bd = sw128_desc(b_tile + kb * BN * 128 + kk * 32);
-              mma_bf16(tmem + acc * BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+              const int kb = k / 4, kq = k % 4;
+              const uint64_t ad = sw128_desc(a_tile + kb * BM * 128 + kq * 32);
+              const uint64_t bd = sw128_desc(b_tile + kb * BN * 128 + kq * 32);
+              mma_bf16(tmem + t * BN, ad, bd, idesc, k > 0 ? 1u : 0u);
             }
-            mma_commit(&accfull[acc]);
+            mma_commit(&accfull[t]);
             ++kt[t];
+            if (c == it.n_ch - 1) mma_commit(&aempty[t]);  // slot's A free for the next item
           }
           if (!ok) break;
           mma_commit(&empty[s]);
           ++b_iter;
         }
-        if (ok) mma_commit(&aempty[ab]);
       }
       mma_commit(done);
       drain_wait(done, 0, p.status);
@@ -354,24 +480,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    // Warp 2 + 4g + i (g = 0..3): tile slot g & 1, column half g >> 1 of every
-    // accumulator; lane quarter warp % 4 (the TMEM lanes a warp may access).
-    // Four epilogue warps per SM sub-partition hide each other's TMEM-load and
-    // barrier latency.  The two halves of a row (pass 1) or slot (pass 2)
-    // combine at the end of the item: half 1 stores its partial where the
-    // result goes and signals, half 0 reads it back and writes the result.
+    // Warp 2 + 4g + i (g = 0..3): tile slot g & 1, column half g >> 1 of the
+    // slot's accumulator; lane quarter warp % 4 (the TMEM lanes a warp may
+    // access).  Four epilogue warps per SM sub-partition hide each other's
+    // TMEM-load and barrier latency.  The two halves of a row (pass 1) or slot
+    // (pass 2) combine at the end of the item: half 1 stores its partial where
+    // the result goes and signals, half 0 reads it back and writes the result.
     const int grp = (warp - 2) >> 2;
-    const int wg = grp & 1;            // A tile slot of the item
-    const int half = grp >> 1;         // accumulator columns [64 half, 64 half + 64)
+    const int wg = grp & 1;            // tile slot
+    const int half = grp >> 1;         // accumulator columns [128 half, 128 half + 128)
     const int quarter = warp & 3;
     const int lrow = quarter * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                            static_cast<uint32_t>(wg * BN + half * kHalf);
     const int tq = wg * 4 + quarter;   // merge barrier pair of this (tile slot, quarter)
     const float c = p.scale_log2;
-    int k = 0;        // accumulators of this tile slot consumed
+    int k = 0;        // accumulator fills of this tile slot consumed
     int n_merge = 0;  // merges of this (tile slot, quarter): both halves count alike
     int rb_iter = 0;
     bool ok = true;
+    auto release = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&accempty[wg]);
+    };
     for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
       const Item it = decode<PASS>(p, item);
       const int tile = wg == 0 ? it.tile[0] : it.tile[1];
@@ -381,76 +513,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_valid = tile >= 0 && (r < p.R) && (qpos >= it.pad) && (it.n_ch > 0);
         float mz = -INFINITY, sum = 0.f;  // max in raw logit units, sum rel. to it
         for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
-          const int acc = wg * 2 + (k & 1);
-          if (!epi_wait(&accfull[acc], (k >> 1) & 1, abort, p.status, lane)) {
+          if (!epi_wait(&accfull[wg], k & 1, abort, p.status, lane)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const int c0 = it.c_start + ch * BN;
-          const int lo = max(it.pad, c0), hi = min(qpos, c0 + BN - 1);
-          const bool fast = __all_sync(0xffffffffu,
-                                       row_valid && lo == c0 && hi == c0 + BN - 1);
-          // this half of the accumulator row into registers, then release it
+          const int n_cols = chunk_cols(it, ch);
+          const int nb = max(0, min(4, (n_cols - half * kHalf) / 32));  // this warp's blocks
+          const int lo = max(it.pad, c0), hi = min(qpos, c0 + n_cols - 1);
+          const int p0 = c0 + half * kHalf;
+          // every row of the warp sees all of this warp's 128 columns
+          const bool fast = __all_sync(0xffffffffu, row_valid && nb == 4 && lo <= p0 &&
+                                                        hi >= p0 + kHalf - 1);
           uint32_t v[2][32];
-          float bmx[2] = {-INFINITY, -INFINITY};
-          const uint32_t ta = t_lane + acc * BN + half * 64;
+          float bmx[2];
           __syncwarp();
-          if (fast) {
-            tmem_ld32_max(ta, v[0], bmx[0]);  // block maxima from the load path
-            tmem_ld32_max(ta + 32, v[1], bmx[1]);
+          if (nb == 4 && fast) {
+            // whole half, every row sees every column: two 64-column steps,
+            // release after the second load
+            load2(t_lane, true, v, bmx);
+            tmem_ld_wait();
+            row_block<true>(v[0], bmx[0], p0, lo, hi, c, mz, sum);
+            row_block<true>(v[1], bmx[1], p0 + 32, lo, hi, c, mz, sum);
+            __syncwarp();
+            load2(t_lane + 64, true, v, bmx);
+            tmem_ld_wait();
+            release();
+            row_block<true>(v[0], bmx[0], p0 + 64, lo, hi, c, mz, sum);
+            row_block<true>(v[1], bmx[1], p0 + 96, lo, hi, c, mz, sum);
           } else {
-            tmem_ld32(ta, v[0]);
-            tmem_ld32(ta + 32, v[1]);
+            // masked or partial chunk: one block at a time
+            for (int b = 0; b < nb; ++b) {
+              __syncwarp();
+              tmem_ld32(t_lane + 32 * b, v[0]);
+              tmem_ld_wait();
+              if (b == nb - 1) release();
+              row_block<false>(v[0], -INFINITY, p0 + 32 * b, lo, hi, c, mz, sum);
+            }
+            if (nb == 0) release();
           }
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[acc]);
           ++k;
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            // masked columns (padding, not yet seen by the row) drop out by select
-            const int p0 = c0 + (half * 2 + b) * 32;
-            float bm = bmx[b];
-            if (!fast) {
-              bm = -INFINITY;
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (p0 + i >= lo && p0 + i <= hi) bm = fmaxf(bm, __uint_as_float(v[b][i]));
-            }
-            // online rescale, only when some row's maximum grew (warp-uniform test)
-            if (__any_sync(0xffffffffu, bm > mz)) {
-              const float sc = bm > mz ? ex2((mz - bm) * c) : 1.f;
-              sum *= sc;
-              mz = fmaxf(mz, bm);
-            }
-            const float neg = -mz * c;
-            float e[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2)
-              fma2(e[i], e[i + 1], __uint_as_float(v[b][i]), __uint_as_float(v[b][i + 1]), c, c,
-                   neg, neg);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) e[i] = ex2(e[i]);
-            if (!fast) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) e[i] = (p0 + i >= lo && p0 + i <= hi) ? e[i] : 0.f;
-            }
-#pragma unroll
-            for (int w = 16; w >= 2; w >>= 1)
-#pragma unroll
-              for (int i = 0; i < w; i += 2)
-                add2(e[i], e[i + 1], e[i], e[i + 1], e[i + w], e[i + w + 1]);
-            sum += e[0] + e[1];
-          }
         }
         if (!ok) break;
         if (tile < 0) continue;
         const size_t o = static_cast<size_t>(it.u) * p.Rp + r;
         const bool in_rows = r < p.Rp;
         if (half == 1) {
-          // partial (max, sum) of columns [64, 128) of every chunk
+          // partial (max, sum) of columns [128, 256) of every chunk
           if (!epi_wait(&mrg_empty[tq], (n_merge & 1) ^ 1, abort, p.status, lane)) break;
           if (in_rows) {
             p.negb[o] = mz;
@@ -488,66 +598,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool pos_valid = tile >= 0 && (pos >= it.pad) && (pos < p.T);
         const bool fast = __all_sync(0xffffffffu, pos_valid && (pos <= p.T - p.W));
         const int jmin = pos - (p.T - p.W);  // rows with j >= jmin see pos
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
         for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
-          const int acc = wg * 2 + (k & 1);
-          if (!epi_wait(&accfull[acc], (k >> 1) & 1, abort, p.status, lane)) {
+          if (!epi_wait(&accfull[wg], k & 1, abort, p.status, lane)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const int n_cols = chunk_cols(it, ch);
+          const int nb = max(0, min(4, (n_cols - half * kHalf) / 32));
+          const int r0 = ch * BN + half * kHalf;  // first query row of this warp's columns
           uint32_t v[2][32];
-          const uint32_t ta = t_lane + acc * BN + half * 64;
+          float bmx[2];
           __syncwarp();
-          tmem_ld32(ta, v[0]);
-          tmem_ld32(ta + 32, v[1]);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[acc]);
-          ++k;
-#pragma unroll
-          for (int b = 0; b < 2; ++b) {
-            const int r0 = ch * BN + (half * 2 + b) * 32;  // first query row of the block
-            const float* rbb = row_b + r0;
-            float e[32];
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 nb = lds128(rbb + i);  // negated row constants (-inf past R)
-              fma2(e[i], e[i + 1], __uint_as_float(v[b][i]), __uint_as_float(v[b][i + 1]), c, c,
-                   nb.x, nb.y);
-              fma2(e[i + 2], e[i + 3], __uint_as_float(v[b][i + 2]),
-                   __uint_as_float(v[b][i + 3]), c, c, nb.z, nb.w);
+          if (nb == 4 && fast) {
+            // whole half, every query row sees the slot
+            load2(t_lane, false, v, bmx);
+            tmem_ld_wait();
+            slot_block<true>(v[0], row_b + r0, r0, p.W, jmin, c, acc);
+            slot_block<true>(v[1], row_b + r0 + 32, r0 + 32, p.W, jmin, c, acc);
+            __syncwarp();
+            load2(t_lane + 64, false, v, bmx);
+            tmem_ld_wait();
+            release();
+            slot_block<true>(v[0], row_b + r0 + 64, r0 + 64, p.W, jmin, c, acc);
+            slot_block<true>(v[1], row_b + r0 + 96, r0 + 96, p.W, jmin, c, acc);
+          } else {
+            for (int b = 0; b < nb; ++b) {
+              __syncwarp();
+              tmem_ld32(t_lane + 32 * b, v[0]);
+              tmem_ld_wait();
+              if (b == nb - 1) release();
+              slot_block<false>(v[0], row_b + r0 + 32 * b, r0 + 32 * b, p.W, jmin, c, acc);
             }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) e[i] = ex2(e[i]);
-            if (!fast) {
-              // window query j sees this slot only if j >= jmin
-              int j = r0 % p.W;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                e[i] = j >= jmin ? e[i] : 0.f;
-                j = (j + 1 == p.W) ? 0 : j + 1;
-              }
-            }
-#pragma unroll
-            for (int w = 16; w >= 4; w >>= 1)
-#pragma unroll
-              for (int i = 0; i < w; i += 2)
-                add2(e[i], e[i + 1], e[i], e[i + 1], e[i + w], e[i + w + 1]);
-            add2(a0, a1, a0, a1, e[0], e[1]);
-            add2(a2, a3, a2, a3, e[2], e[3]);
+            if (nb == 0) release();
           }
+          ++k;
         }
         // every epilogue warp releases the row constants, tile or no tile
         __syncwarp();
         if (lane == 0) mbar_arrive(&rbempty[rb]);
         if (!ok) break;
         if (tile < 0) continue;
-        const float part = (a0 + a1) + (a2 + a3);
+        const float part = acc.x + acc.y;
         float* dst = p.usage + static_cast<size_t>(it.u) * p.T + pos;
         if (half == 1) {
-          // partial usage over the query rows of columns [64, 128) of every chunk
+          // partial usage over the query rows of columns [128, 256) of every chunk
           if (!epi_wait(&mrg_empty[tq], (n_merge & 1) ^ 1, abort, p.status, lane)) break;
           if (pos_valid) *dst = part;
           __threadfence_block();
@@ -598,16 +694,18 @@ EncodeTiledFn get_encode(std::string* err) {
 }
 
 // 3-D view of a [rows][d] bf16 tensor: x = 64 elements of a K block (128 B),
-// y = row (stride d*2 B), z = K block (stride 128 B).  A box of 64 x 128 x d/64
-// lands in shared memory as d/64 consecutive [128 rows][128 B] blocks, each
-// with the 128-byte swizzle -- the K-major layout the MMA descriptors expect --
-// in a single TMA operation.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int d, std::string* err) {
+// y = row (stride d*2 B), z = K block (stride 128 B).  A box of
+// 64 x box_rows x d/64 lands in shared memory as d/64 consecutive
+// [box_rows][128 B] blocks, each with the 128-byte swizzle -- the K-major
+// layout the MMA descriptors expect -- in a single TMA operation.  Rows past
+// the end of the tensor read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int d, int box_rows,
+              std::string* err) {
   EncodeTiledFn enc = get_encode(err);
   if (!enc) return false;
   cuuint64_t dims[3] = {64, rows, static_cast<cuuint64_t>(d / 64)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, 128};
-  cuuint32_t box[3] = {64, 128, static_cast<cuuint32_t>(d / 64)};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(d / 64)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -631,12 +729,10 @@ int smem_optin() {
   return v;
 }
 
-// A buffers (items in flight) and B-ring depth: two A buffers (the next item's
-// operands load while the current item runs) with the deepest ring that fits.
-constexpr int kAbuf = 2;
-int pick_stages(int D, int rbf, int n_abuf) {
+// The deepest B ring (at least 2 stages) that fits next to the A tiles.
+int pick_stages(int D, int rbf) {
   for (int s = kMaxStages; s >= 2; --s)
-    if (Layout(D, s, rbf, n_abuf).total <= smem_optin()) return s;
+    if (Layout(D, s, rbf).total <= smem_optin()) return s;
   return 0;
 }
 
@@ -644,9 +740,13 @@ template <int D>
 cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStream_t s,
                      std::string* err) {
   const Dims& dm = h->dims;
-  CUtensorMap map_q, map_k;
-  if (!make_map(&map_q, a.q, static_cast<uint64_t>(dm.U) * dm.R, D, err) ||
-      !make_map(&map_k, a.k, static_cast<uint64_t>(dm.U) * a.T, D, err))
+  const uint64_t q_rows = static_cast<uint64_t>(dm.U) * dm.R;
+  const uint64_t k_rows = static_cast<uint64_t>(dm.U) * a.T;
+  // pass 1: A = query tiles (128 rows), B = key chunks (256 rows);
+  // pass 2: A = key tiles, B = query chunks
+  CUtensorMap map_a, map_b;
+  if (!make_map(&map_a, pass == 1 ? a.q : a.k, pass == 1 ? q_rows : k_rows, D, BM, err) ||
+      !make_map(&map_b, pass == 1 ? a.k : a.q, pass == 1 ? k_rows : q_rows, D, BN, err))
     return cudaErrorInvalidValue;
 
   Params p;
@@ -665,13 +765,12 @@ cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStre
   p.status = h->ws.status;
 
   const int rbf = (pass == 2) ? rowb_floats(dm.R) : 0;
-  p.n_abuf = kAbuf;
-  p.n_stages = pick_stages(D, rbf, p.n_abuf);
+  p.n_stages = pick_stages(D, rbf);
   if (p.n_stages == 0) {
     if (err) *err = "attention kernel does not fit in shared memory";
     return cudaErrorInvalidValue;
   }
-  const size_t smem = Layout(D, p.n_stages, rbf, p.n_abuf).total;
+  const size_t smem = Layout(D, p.n_stages, rbf).total;
   p.n_tiles = (pass == 1) ? (dm.R + BM - 1) / BM : (a.T + BM - 1) / BM;
   p.n_pairs = (p.n_tiles + kTiles - 1) / kTiles;
   p.n_items = dm.U * p.n_pairs;
@@ -682,12 +781,12 @@ cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStre
     e = cudaFuncSetAttribute(usage_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    usage_kernel<D, 1><<<grid, kThreads, smem, s>>>(map_q, map_k, p);
+    usage_kernel<D, 1><<<grid, kThreads, smem, s>>>(map_a, map_b, p);
   } else {
     e = cudaFuncSetAttribute(usage_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    usage_kernel<D, 2><<<grid, kThreads, smem, s>>>(map_k, map_q, p);
+    usage_kernel<D, 2><<<grid, kThreads, smem, s>>>(map_a, map_b, p);
   }
   return cudaGetLastError();
 }
@@ -709,7 +808,7 @@ cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a, int 
 
 // Shared memory the attention kernels need with their shallowest ring (2 stages).
 size_t attention_usage_smem_bytes(int d, int R) {
-  return static_cast<size_t>(Layout(d, 2, rowb_floats(R), kAbuf).total);
+  return static_cast<size_t>(Layout(d, 2, rowb_floats(R)).total);
 }
 
 int attention_row_stride(int R) { return round4(R); }

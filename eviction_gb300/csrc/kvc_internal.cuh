@@ -176,6 +176,26 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_test, but a thread whose phase is not complete yet is suspended
+// until it completes or about `hint_ns` have passed (it does not spin and so
+// leaves the issue slots of its SM sub-partition to the other warps).
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity,
+                                                uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Suspension hint of one wait step: short enough that the abort flag and the
+// time limit are checked often.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
 // after kWaitLimitNs or as soon as *abort becomes non-zero; returns false then
 // (and on its own time-out raises *abort and the device status bit).
@@ -185,7 +205,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       *abort = 1;
@@ -351,24 +371,9 @@ __device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32],
       : "memory");
 }
 
-// Packed pair arithmetic (two fp32 lanes per instruction).
-__device__ __forceinline__ void fma2(float& dx, float& dy, float ax, float ay, float bx,
-                                     float by, float cx, float cy) {
-  asm("{\n\t.reg .b64 a, b, c, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
-      "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(dx), "=f"(dy)
-      : "f"(ax), "f"(ay), "f"(bx), "f"(by), "f"(cx), "f"(cy));
-}
-
-__device__ __forceinline__ void add2(float& dx, float& dy, float ax, float ay, float bx,
-                                     float by) {
-  asm("{\n\t.reg .b64 a, b, d;\n\t"
-      "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-      "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(dx), "=f"(dy)
-      : "f"(ax), "f"(ay), "f"(bx), "f"(by));
-}
+// Packed pair arithmetic (two fp32 lanes per instruction, FFMA2 / FADD2).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
