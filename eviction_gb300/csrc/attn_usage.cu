@@ -276,6 +276,66 @@ __device__ __forceinline__ void slot_block(const uint32_t (&v)[32], const float*
   acc = add2(acc, e[0]);
 }
 
+// Both blocks of a fully visible 64-column step at once (pass 1): one rescale
+// decision for the pair, then 64 independent exponentials and one sum tree.
+__device__ __forceinline__ void row_pair(const uint32_t (&v)[2][32], const float (&bmx)[2],
+                                         float c, float& mz, float& sum) {
+  const float bm = fmaxf(bmx[0], bmx[1]);
+  if (__any_sync(0xffffffffu, bm > mz)) {
+    const float sc = bm > mz ? ex2((mz - bm) * c) : 1.f;
+    sum *= sc;
+    mz = fmaxf(mz, bm);
+  }
+  const float neg = -mz * c;
+  const float2 cc = make_float2(c, c), nn = make_float2(neg, neg);
+  float2 e[32];
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      e[16 * b + i] = fma2(make_float2(__uint_as_float(v[b][2 * i]),
+                                       __uint_as_float(v[b][2 * i + 1])), cc, nn);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    e[i].x = ex2(e[i].x);
+    e[i].y = ex2(e[i].y);
+  }
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) e[i] = add2(e[i], e[i + w]);
+  sum += e[0].x + e[0].y;
+}
+
+// Both blocks of a 64-row step seen by every query row (pass 2).
+__device__ __forceinline__ void slot_pair(const uint32_t (&v)[2][32], const float* rbb, float c,
+                                          float2& acc) {
+  const float2 cc = make_float2(c, c);
+  float2 e[32];
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      const float4 nb = lds128(rbb + 32 * b + 2 * i);  // negated row constants (-inf past R)
+      e[16 * b + i] = fma2(make_float2(__uint_as_float(v[b][2 * i]),
+                                       __uint_as_float(v[b][2 * i + 1])), cc,
+                           make_float2(nb.x, nb.y));
+      e[16 * b + i + 1] = fma2(make_float2(__uint_as_float(v[b][2 * i + 2]),
+                                           __uint_as_float(v[b][2 * i + 3])), cc,
+                               make_float2(nb.z, nb.w));
+    }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    e[i].x = ex2(e[i].x);
+    e[i].y = ex2(e[i].y);
+  }
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) e[i] = add2(e[i], e[i + w]);
+  acc = add2(acc, e[0]);
+}
+
 // Copy two 32-column blocks of this warp's accumulator rows to registers,
 // with the per-block maxima from the load path when `with_max` (warp-uniform).
 __device__ __forceinline__ void load2(uint32_t taddr, bool with_max, uint32_t (&v)[2][32],
@@ -534,14 +594,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // release after the second load
             load2(t_lane, true, v, bmx);
             tmem_ld_wait();
-            row_block<true>(v[0], bmx[0], p0, lo, hi, c, mz, sum);
-            row_block<true>(v[1], bmx[1], p0 + 32, lo, hi, c, mz, sum);
+            row_pair(v, bmx, c, mz, sum);
             __syncwarp();
             load2(t_lane + 64, true, v, bmx);
             tmem_ld_wait();
             release();
-            row_block<true>(v[0], bmx[0], p0 + 64, lo, hi, c, mz, sum);
-            row_block<true>(v[1], bmx[1], p0 + 96, lo, hi, c, mz, sum);
+            row_pair(v, bmx, c, mz, sum);
           } else {
             // masked or partial chunk: one block at a time
             for (int b = 0; b < nb; ++b) {
@@ -615,14 +673,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // whole half, every query row sees the slot
             load2(t_lane, false, v, bmx);
             tmem_ld_wait();
-            slot_block<true>(v[0], row_b + r0, r0, p.W, jmin, c, acc);
-            slot_block<true>(v[1], row_b + r0 + 32, r0 + 32, p.W, jmin, c, acc);
+            slot_pair(v, row_b + r0, c, acc);
             __syncwarp();
             load2(t_lane + 64, false, v, bmx);
             tmem_ld_wait();
             release();
-            slot_block<true>(v[0], row_b + r0 + 64, r0 + 64, p.W, jmin, c, acc);
-            slot_block<true>(v[1], row_b + r0 + 96, r0 + 96, p.W, jmin, c, acc);
+            slot_pair(v, row_b + r0 + 64, c, acc);
           } else {
             for (int b = 0; b < nb; ++b) {
               __syncwarp();
