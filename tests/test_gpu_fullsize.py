@@ -14,9 +14,9 @@ benchmark times, checked on sampled units that the oracle recomputes one by one.
     against the oracle on both layouts;
   * long (T = 32768, 448 units): 2 sampled units.
 Per unit (tests.gpu_util.check_unit_e2e): mass and score within 1e-4 relative,
-the oracle's integer steps fed the GPU's fp32 mass/score reproduce the GPU's
-kept set bit-exactly, and the oracle's own kept set matches up to near-ties or a
-cut that moved at a threshold; compaction is exact for the GPU's indices.
+and the oracle's own kept set matches the GPU's up to near-ties or a cut that
+moved at a threshold (GPU segments from the GPU's own kernel; no GPU value is
+ever an oracle input); compaction is exact for the GPU's indices.
 """
 import numpy as np
 import pytest
@@ -51,7 +51,8 @@ def _unit_inputs(inp, units):
 
 
 def _run(h, inp):
-    """kvc_event plus kvc_mass (for the stage values) on the same inputs."""
+    """kvc_event plus kvc_mass and kvc_segment_quota (for the stage values) on the
+    same inputs."""
     T = inp.T
     out = h.outputs(T)
     h.event(inp.q, inp.k, inp.v, T, inp.pad, inp.n_carry, inp.credit, out["k_out"],
@@ -59,6 +60,8 @@ def _run(h, inp):
     st = h.stage_buffers(T)
     h.mass(inp.q, inp.k, T, inp.pad, inp.n_carry, inp.credit, st["credit_post"], st["mass"],
            st["score"])
+    h.segment_quota(st["mass"], T, inp.pad, st["seg_start"], st["seg_len"], st["quota"],
+                    st["n_seg"])
     torch.cuda.synchronize()
     assert h.device_status() == 0
     return out, st
@@ -81,9 +84,11 @@ def _check(ref, p, w, inp, out, st, units, r, rows=None):
         n = int(nk[u])
         assert n == int(r["n_kept"][row])
         g = kept[u, :n].cpu().numpy()
-        verdicts.append(gu.check_unit_e2e(ref, p, w, int(pads[u]), g,
+        seg = {k2: st[k2].reshape(U, -1)[u].cpu().numpy() for k2 in ("seg_start", "seg_len", "quota")}
+        seg["n_seg"] = int(st["n_seg"].reshape(U)[u])
+        verdicts.append(gu.check_unit_e2e(p, w, int(pads[u]), g,
                                           st["mass"].reshape(U, T)[u].cpu().numpy(),
-                                          st["score"].reshape(U, T)[u].cpu().numpy(), r, row))
+                                          st["score"].reshape(U, T)[u].cpu().numpy(), seg, r, row))
         ok_c, rel_c = gu.mass_close(c_post[u].cpu().numpy(), r["credit_post"][row])
         assert ok_c, f"unit {u}: credit rel {rel_c:.3g}"
         idx = torch.as_tensor(g, dtype=torch.long, device=k_src.device)
