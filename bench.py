@@ -37,6 +37,15 @@ if ROOT not in sys.path:
 METRIC = "cached tokens scanned/s per compression event"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The pages' ablations as library switches ("none" = the method).
+ABLATIONS = {
+    "none": {},
+    "fixed_segments": {"seg_fixed": 64},
+    "no_mass_quota": {"quota_by_len": 1},
+    "no_credit": {"beta": 1.0},
+    "global_topk": {"global_topk": 1},
+}
+
 KERNEL_SOURCES = {
     "usage_pass1_rowstats_tcgen05": "attn_usage.cu",
     "usage_pass2_colsum_tcgen05": "attn_usage.cu",
@@ -60,6 +69,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ablation", choices=sorted(ABLATIONS), default="none",
+                    help="time one of the method's ablations (the pages' ablation table)")
     return ap.parse_args()
 
 
@@ -225,7 +236,7 @@ def run_reference(args, w):
     sample_w = wl.scaled(w, n_layers=1, batch=1)
     first = wl.generate(sample_w, device="cpu")
     p = oracle.RefParams(group=w.group, head_dim=w.head_dim, window=w.window, budget=w.budget,
-                         n_sink=w.n_sink, n_recent=w.n_recent)
+                         n_sink=w.n_sink, n_recent=w.n_recent, **ABLATIONS[args.ablation])
 
     def unit_inputs(inp):
         return (wl.bf16_bits(wl.q_units(inp.q, inp.w)), wl.bf16_bits(wl.units_of(inp.k, inp.w)),
@@ -270,7 +281,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": workload_config(w, T),
+        "config": workload_config(w, T, args.ablation),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -278,14 +289,17 @@ def run_reference(args, w):
     print(json.dumps(line))
 
 
-def workload_config(w, T):
-    return {"workload": (f"{w.name}: {w.n_layers} layers x batch {w.batch} x {w.n_kv_heads} KV heads"
+def workload_config(w, T, ablation="none"):
+    cfg = {"workload": (f"{w.name}: {w.n_layers} layers x batch {w.batch} x {w.n_kv_heads} KV heads"
                          f" (GQA {w.group}), d {w.head_dim}, {T} slots -> budget {w.budget}, "
                          f"window {w.window}" + (", event 2 (credit carried, 512 fresh slots)"
                                                  if w.n_events > 1 else "")),
             "units": w.units, "T": T, "budget": w.budget, "window": w.window,
             "group": w.group, "head_dim": w.head_dim,
             "l2": "inputs larger than L2 (no flush needed)"}
+    if ablation != "none":
+        cfg["ablation"] = f"{ablation}: {ABLATIONS[ablation]}"
+    return cfg
 
 
 # ------------------------------------------------------------------ our arm
@@ -311,7 +325,7 @@ def run_ours(args, w):
     T = first.T
     cfg = kvc.Config(w.n_layers, w.batch, w.n_kv_heads, w.group, w.head_dim,
                      max(T, w.budget + w.interval), w.budget, window=w.window, n_sink=w.n_sink,
-                     n_recent=w.n_recent)
+                     n_recent=w.n_recent, **ABLATIONS[args.ablation])
     h = kvc.Handle(cfg)
     inp = first
     if w.n_events > 1:
@@ -445,7 +459,8 @@ def run_ours(args, w):
         import oracle
         oracle.build()
         p = oracle.RefParams(group=w.group, head_dim=w.head_dim, window=w.window,
-                             budget=w.budget, n_sink=w.n_sink, n_recent=w.n_recent)
+                             budget=w.budget, n_sink=w.n_sink, n_recent=w.n_recent,
+                             **ABLATIONS[args.ablation])
         q_u = wl.q_units(inp.q, w)
         k_u = wl.units_of(inp.k, w)
         v_u = wl.units_of(inp.v, w)
@@ -474,7 +489,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w, T), parallelism=f"replicas x{world}"),
+        "config": dict(workload_config(w, T, args.ablation), parallelism=f"replicas x{world}"),
         "roofline": roofline, "event_roofline": event_roofline,
         "kernels": [{k2: (round(v, 6) if isinstance(v, float) else v) for k2, v in r.items()}
                     for r in krows],

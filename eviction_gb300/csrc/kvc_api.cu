@@ -53,6 +53,11 @@ int validate_config(const kvc_config* c, std::string* why) {
   if (!(c->eps > 0.f) || !std::isfinite(c->eps)) return bad("eps must be finite and > 0");
   if (!(c->softmax_scale >= 0.f) || !std::isfinite(c->softmax_scale))
     return bad("softmax_scale must be finite and >= 0");
+  if (c->seg_fixed < 0 || (c->seg_fixed > 0 && c->seg_fixed < c->seg_min))
+    return bad("seg_fixed must be 0 or >= seg_min");
+  if ((c->quota_by_len != 0 && c->quota_by_len != 1) ||
+      (c->global_topk != 0 && c->global_topk != 1))
+    return bad("quota_by_len and global_topk must be 0 or 1");
   if (c->head_dim != 64 && c->head_dim != 128) {
     *why = "head_dim must be 64 or 128";
     return KVC_ERR_UNSUPPORTED;

@@ -51,6 +51,7 @@ __device__ __forceinline__ uint64_t warp_incl_scan(uint64_t v) {
 struct SegParams {
   int T, B, H, S_max, S_cap;
   int budget, q_min, seg_min, seg_max;
+  int seg_fixed, quota_by_len, global_topk;  // ablation switches (0 = the method)
   double delta;
   int K;  // number of thresholds
   const float* mass;
@@ -290,7 +291,22 @@ __global__ void __launch_bounds__(kThreads)
   __syncthreads();
 
   // ---- 3. raw segments, merge, split (serial: at most K+1 raw segments)
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && (p.global_topk || p.seg_fixed > 0)) {
+    // ablations: one segment over everything, or fixed-length segments whose
+    // shorter tail joins the segment before it
+    int ns_ab = 1;
+    if (p.global_topk) {
+      s_start[0] = 0;
+      s_len[0] = n;
+    } else {
+      ns_ab = max(1, n / p.seg_fixed);
+      for (int s = 0; s < ns_ab; ++s) {
+        s_start[s] = s * p.seg_fixed;
+        s_len[s] = (s + 1 < ns_ab) ? p.seg_fixed : n - s * p.seg_fixed;
+      }
+    }
+    s_nseg = ns_ab;
+  } else if (threadIdx.x == 0) {
     // raw segments into s_start/s_len (drop empty)
     int n_raw = 0, prev = 0;
     for (int k = 0; k < p.K; ++k) {
@@ -366,6 +382,11 @@ __global__ void __launch_bounds__(kThreads)
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) s_mass[s] = acc;
   }
+  __syncthreads();
+
+  // ablation: quotas in proportion to segment length (lengths replace masses)
+  if (p.quota_by_len)
+    for (int s = threadIdx.x; s < ns; s += kThreads) s_mass[s] = static_cast<uint64_t>(s_len[s]);
   __syncthreads();
 
   // ---- 5. quotas (warp 0)
@@ -468,8 +489,11 @@ int segment_capacity(const kvc_config& c, int T) {
   // most min(S_max, K + 1 + ceil(T/seg_max)).
   const int bound = K + 1 + (T + c.seg_max - 1) / c.seg_max;
   const int smax = s_max_of(c, T);
-  const int after = bound < smax ? bound : smax;
-  return after > K + 1 ? after : K + 1;
+  int cap = bound < smax ? bound : smax;
+  if (cap < K + 1) cap = K + 1;
+  // fixed-length ablation: at most T / seg_fixed (<= T / seg_min) segments
+  if (c.seg_fixed > 0 && T / c.seg_fixed > cap) cap = T / c.seg_fixed;
+  return cap;
 }
 
 size_t segment_smem_bytes(const kvc_config& c, int T) {
@@ -491,6 +515,9 @@ cudaError_t launch_segment_quota(const kvc_handle* h, const float* mass, int T,
   p.q_min = c.q_min;
   p.seg_min = c.seg_min;
   p.seg_max = c.seg_max;
+  p.seg_fixed = c.seg_fixed;
+  p.quota_by_len = c.quota_by_len;
+  p.global_topk = c.global_topk;
   p.delta = static_cast<double>(c.delta);
   p.K = segment_threshold_count(p.delta);
   p.mass = mass;

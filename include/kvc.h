@@ -101,6 +101,17 @@ typedef struct {
   float beta;      /* current-mass weight in [0,1] (0.9)                   */
   float eps;       /* mass floor > 0 (1e-6)                                */
   float softmax_scale; /* 0 => 1/sqrt(head_dim)                            */
+  /* Ablation switches ("Adaptive Mass-Segmented KV Compression for Long-Form
+   * Reasoning", Experiments, ablation table: fixed-length segments, no
+   * mass-weighted quota, global head-only top-k; "no EMA credit" is
+   * beta = 1).  All 0 = the method.                                        */
+  int seg_fixed;     /* > 0: segments of seg_fixed valid slots (>= seg_min)
+                        instead of mass cut points; a shorter tail joins the
+                        segment before it                                   */
+  int quota_by_len;  /* 1: quotas in proportion to segment length instead of
+                        segment mass (same minimums, rounding, correction)  */
+  int global_topk;   /* 1: one segment over all valid slots, quota = budget:
+                        per-head top-k on the score plus the must-keep set  */
 } kvc_config;
 
 typedef struct kvc_handle kvc_handle;

@@ -49,7 +49,8 @@ class _Cfg(ctypes.Structure):
         ("delta", ctypes.c_float), ("seg_min", ctypes.c_int), ("seg_max", ctypes.c_int),
         ("q_min", ctypes.c_int), ("n_sink", ctypes.c_int), ("n_recent", ctypes.c_int),
         ("lambda_", ctypes.c_float), ("beta", ctypes.c_float), ("eps", ctypes.c_float),
-        ("softmax_scale", ctypes.c_float),
+        ("softmax_scale", ctypes.c_float), ("seg_fixed", ctypes.c_int),
+        ("quota_by_len", ctypes.c_int), ("global_topk", ctypes.c_int),
     ]
 
 
@@ -72,12 +73,15 @@ class RefParams:
     beta: float = 0.9
     eps: float = 1e-6
     softmax_scale: float = 0.0
+    seg_fixed: int = 0       # ablation: fixed-length segments
+    quota_by_len: int = 0    # ablation: quotas by length
+    global_topk: int = 0     # ablation: one segment per unit
 
     def c(self) -> _Cfg:
         return _Cfg(self.group, self.head_dim, self.window, self.budget, self.avg_pool,
                     self.max_pool, self.delta, self.seg_min, self.seg_max, self.q_min,
                     self.n_sink, self.n_recent, self.lam, self.beta, self.eps,
-                    self.softmax_scale)
+                    self.softmax_scale, self.seg_fixed, self.quota_by_len, self.global_topk)
 
 
 def lib():
@@ -102,6 +106,8 @@ def _declare(L):
     L.kvc_ref_boundaries.restype = _I
     L.kvc_ref_segments.argtypes = [_P, _I, _I, ctypes.c_float, _I, _I, _P, _P, _P]
     L.kvc_ref_segments.restype = _I
+    L.kvc_ref_segments_ablation.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P]
+    L.kvc_ref_segments_ablation.restype = _I
     L.kvc_ref_quotas.argtypes = [_P, _P, _I, _I, _I, _P]
     L.kvc_ref_select_unit.argtypes = [_P, _I, _I, _P, _P, _P, _I, _I, _I, _I, _P]
     L.kvc_ref_select_unit.restype = _I
@@ -191,6 +197,20 @@ def segments(m_used, pad=0, delta=0.1, seg_min=16, seg_max=256):
     M = np.zeros(cap, np.uint64)
     ns = lib().kvc_ref_segments(_ptr(m), T, pad, float(delta), seg_min, seg_max,
                                 _ptr(st), _ptr(ln), _ptr(M))
+    return st[:ns].copy(), ln[:ns].copy(), M[:ns].copy()
+
+
+def segments_ablation(m_used, pad=0, seg_fixed=0, global_=0):
+    """Fixed-length (seg_fixed > 0) or single-segment (global_) segmentation:
+    (starts as valid offsets, lengths, fixed-point masses)."""
+    m = _c(m_used, np.float32)
+    T = m.shape[0]
+    cap = max(1, T)
+    st = np.zeros(cap, np.int32)
+    ln = np.zeros(cap, np.int32)
+    M = np.zeros(cap, np.uint64)
+    ns = lib().kvc_ref_segments_ablation(_ptr(m), T, pad, int(seg_fixed), int(global_),
+                                         _ptr(st), _ptr(ln), _ptr(M))
     return st[:ns].copy(), ln[:ns].copy(), M[:ns].copy()
 
 

@@ -341,6 +341,46 @@ int kvc_ref_segments(const float* m_used, int T, int pad, float delta,
   return n_seg;
 }
 
+/*
+ * [AMS] Experiments, ablation table: the method without adaptive cut points
+ * ("fixed-length segments"), without mass-weighted quotas, and as a global
+ * head-only top-k ("no EMA credit" is beta = 1 in kvc_ref_credit).  The pages
+ * name the ablations but not their details.
+ * Readings:
+ *  [R] fixed-length segments: consecutive runs of seg_fixed valid slots from
+ *      the first valid slot; a shorter tail joins the segment before it (a
+ *      single segment when n < seg_fixed); no merge or split;
+ *  [R] global head-only top-k: one segment over all n valid slots, so its
+ *      quota is the whole budget; must-keep and selection are unchanged;
+ *  [R] no mass-weighted quota: kvc_ref_quotas with each segment's length in
+ *      place of its mass (see kvc_ref_segment_quota).
+ */
+int kvc_ref_segments_ablation(const float* m_used, int T, int pad, int seg_fixed,
+                              int global, int32_t* seg_start, int32_t* seg_len,
+                              uint64_t* seg_mass) {
+  const int n = T - pad;
+  if (n <= 0) return 0;
+  int n_seg = 1;
+  if (global) {
+    seg_start[0] = 0;
+    seg_len[0] = n;
+  } else {
+    n_seg = n / seg_fixed;
+    if (n_seg < 1) n_seg = 1;
+    for (int s = 0; s < n_seg; ++s) {
+      seg_start[s] = s * seg_fixed;
+      seg_len[s] = (s + 1 < n_seg) ? seg_fixed : n - s * seg_fixed;
+    }
+  }
+  for (int s = 0; s < n_seg; ++s) {
+    uint64_t M = 0;
+    for (int v = seg_start[s]; v < seg_start[s] + seg_len[s]; ++v)
+      M += fixed_mass(m_used[pad + v]);
+    seg_mass[s] = M;
+  }
+  return n_seg;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Step 4: quotas                                                             */
 /* ------------------------------------------------------------------------ */
@@ -614,8 +654,14 @@ int kvc_ref_segment_quota(const kvc_ref_config* cfg, int U, int T,
       ln[s] = 0;
       qu[s] = 0;
     }
-    const int ns = kvc_ref_segments(mass + (size_t)unit * T, T, p, cfg->delta,
-                                    cfg->seg_min, cfg->seg_max, st, ln, M);
+    const int ns = (cfg->global_topk || cfg->seg_fixed > 0)
+                       ? kvc_ref_segments_ablation(mass + (size_t)unit * T, T, p,
+                                                   cfg->seg_fixed, cfg->global_topk, st,
+                                                   ln, M)
+                       : kvc_ref_segments(mass + (size_t)unit * T, T, p, cfg->delta,
+                                          cfg->seg_min, cfg->seg_max, st, ln, M);
+    if (cfg->quota_by_len)
+      for (int s = 0; s < ns; ++s) M[s] = (uint64_t)ln[s];
     const int n = T - p;
     const int budget_eff = cfg->budget < n ? cfg->budget : n;
     kvc_ref_quotas(ln, M, ns, budget_eff, cfg->q_min, qu);

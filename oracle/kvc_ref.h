@@ -54,6 +54,9 @@ typedef struct {
   float beta;       /* weight of the current mass in the mix (0.9)        */
   float eps;        /* mass floor (1e-6)                                  */
   float softmax_scale; /* 0 => 1/sqrt(head_dim)                           */
+  int seg_fixed;    /* ablation: > 0 = fixed-length segments               */
+  int quota_by_len; /* ablation: 1 = quotas by segment length, not mass    */
+  int global_topk;  /* ablation: 1 = one segment over all valid slots      */
 } kvc_ref_config;
 
 /* ---- per-unit steps, fp64 (for the pins) -------------------------------- */
@@ -97,6 +100,13 @@ int kvc_ref_boundaries(const float* m_used, int T, int pad, float delta,
 int kvc_ref_segments(const float* m_used, int T, int pad, float delta,
                      int seg_min, int seg_max, int32_t* seg_start,
                      int32_t* seg_len, uint64_t* seg_mass);
+
+/* Ablations of [AMS] (Experiments, ablation table): fixed-length segments
+ * (seg_fixed > 0) or one segment over all valid slots (global != 0), with the
+ * masses recounted as in kvc_ref_segments.  Returns the segment count. */
+int kvc_ref_segments_ablation(const float* m_used, int T, int pad, int seg_fixed,
+                              int global, int32_t* seg_start, int32_t* seg_len,
+                              uint64_t* seg_mass);
 
 /* Step 4 (quotas): exact-integer quotas summing to min(budget, n). */
 void kvc_ref_quotas(const int32_t* seg_len, const uint64_t* seg_mass,
