@@ -37,14 +37,7 @@ if ROOT not in sys.path:
 METRIC = "cached tokens scanned/s per compression event"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# The pages' ablations as library switches ("none" = the method).
-ABLATIONS = {
-    "none": {},
-    "fixed_segments": {"seg_fixed": 64},
-    "no_mass_quota": {"quota_by_len": 1},
-    "no_credit": {"beta": 1.0},
-    "global_topk": {"global_topk": 1},
-}
+from eviction_gb300.kvc import ABLATIONS  # noqa: E402  (the pages' ablations as switches)
 
 KERNEL_SOURCES = {
     "usage_pass1_rowstats_tcgen05": "attn_usage.cu",

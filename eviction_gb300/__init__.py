@@ -6,8 +6,8 @@ with the same entry-point names that takes torch tensors and passes their device
 pointers and the current CUDA stream. There is no CPU fallback: every call fails
 loudly if the library or a CUDA device is missing.
 """
-from .kvc import (Config, Handle, KvcError, library_path, load_library, mass_noalloc,  # noqa: F401
-                  ENTRY_POINTS)
+from .kvc import (ABLATIONS, Config, Handle, KvcError, library_path, load_library,  # noqa: F401
+                  mass_noalloc, ENTRY_POINTS)
 
-__all__ = ["Config", "Handle", "KvcError", "library_path", "load_library", "mass_noalloc",
-           "ENTRY_POINTS"]
+__all__ = ["ABLATIONS", "Config", "Handle", "KvcError", "library_path", "load_library",
+           "mass_noalloc", "ENTRY_POINTS"]

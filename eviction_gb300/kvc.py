@@ -49,6 +49,17 @@ class _CConfig(ctypes.Structure):
                 ("quota_by_len", ctypes.c_int), ("global_topk", ctypes.c_int)]
 
 
+# The ablations of the method's ablation table as Config keyword switches
+# ("none" = the method; "no_credit" sets beta = 1, which turns the credit mix off).
+ABLATIONS = {
+    "none": {},
+    "fixed_segments": {"seg_fixed": 64},
+    "no_mass_quota": {"quota_by_len": 1},
+    "no_credit": {"beta": 1.0},
+    "global_topk": {"global_topk": 1},
+}
+
+
 @dataclass
 class Config:
     """Mirror of kvc_config (defaults: the method's schedule values)."""

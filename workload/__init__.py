@@ -145,7 +145,8 @@ def _region_profile(w: Workload, g, device, B, H, T, lo, span_end):
     diff = torch.zeros((B, H, T + 1), device=device)
     diff.scatter_add_(2, start, amp)
     diff.scatter_add_(2, start + length, -amp)
-    return torch.cumsum(diff, dim=2)[:, :, :T]
+    regions = (start, length, (active > 0) & (length > 0))
+    return torch.cumsum(diff, dim=2)[:, :, :T], regions
 
 
 def _layer(w: Workload, g, device, T, lengths, region_lo_offset=None):
@@ -160,38 +161,47 @@ def _layer(w: Workload, g, device, T, lengths, region_lo_offset=None):
         lo = pad + w.n_sink
     else:
         lo = torch.full_like(pad, region_lo_offset)
-    amp = _region_profile(w, g, device, B, H, T, lo, torch.full_like(pad, T - w.n_recent))
+    amp, regions = _region_profile(w, g, device, B, H, T, lo, torch.full_like(pad, T - w.n_recent))
     k = k + amp.unsqueeze(-1) * math.sqrt(d) * u_hat.unsqueeze(2)
     slot = torch.arange(T, device=device).view(1, 1, T, 1)
     valid = slot >= pad.view(B, 1, 1, 1)
     k = torch.where(valid, k, torch.zeros((), device=device)).to(torch.bfloat16)
     v = torch.where(valid, v, torch.zeros((), device=device)).to(torch.bfloat16)
-    return q, k, v
+    return q, k, v, regions
 
 
-def generate(w: Workload, device="cpu", seed: Optional[int] = None) -> Inputs:
-    """First-event inputs of workload `w` on `device`."""
+def _stack_regions(regs):
+    """[(start, length, active) per layer] -> dict of [L, B, H, R] tensors."""
+    return {"start": torch.stack([r[0] for r in regs]), "length": torch.stack([r[1] for r in regs]),
+            "active": torch.stack([r[2] for r in regs])}
+
+
+def generate(w: Workload, device="cpu", seed: Optional[int] = None, return_regions=False):
+    """First-event inputs of workload `w` on `device` (and, if asked, the planted
+    regions: slot start, length and an active flag, [L, B, H, R] each)."""
     seed = w.seed if seed is None else seed
     lengths = sequence_lengths(w, device)
     T = int(lengths.max().item()) if w.prefill is not None else w.T
     g = _gen(device, seed)
-    qs, ks, vs = [], [], []
+    qs, ks, vs, regs = [], [], [], []
     for _ in range(w.n_layers):
-        q, k, v = _layer(w, g, device, T, lengths)
+        q, k, v, reg = _layer(w, g, device, T, lengths)
         qs.append(q)
         ks.append(k)
         vs.append(v)
+        regs.append(reg)
     q = torch.stack(qs)
     k = torch.stack(ks)
     v = torch.stack(vs)
     pad = (T - lengths).to(torch.int32)
     credit = torch.zeros((w.n_layers, w.batch, w.n_kv_heads, T), dtype=torch.float32,
                          device=device)
-    return Inputs(w, T, q, k, v, credit, pad, (T - pad).to(torch.int32), lengths)
+    inp = Inputs(w, T, q, k, v, credit, pad, (T - pad).to(torch.int32), lengths)
+    return (inp, _stack_regions(regs)) if return_regions else inp
 
 
 def next_event(w: Workload, prev: Inputs, k_out, v_out, credit_out, n_kept, event_index: int,
-               seed: Optional[int] = None) -> Inputs:
+               seed: Optional[int] = None, return_regions=False):
     """Inputs of the next event: the compacted cache plus `interval` fresh slots.
 
     The fresh slots follow the same law (N(0,1) keys with planted regions aligned
@@ -206,13 +216,14 @@ def next_event(w: Workload, prev: Inputs, k_out, v_out, credit_out, n_kept, even
     assert bool((n_kept == Kb).all()), "next_event needs full-budget compaction"
     T = Kb + I
     fresh_w = replace(w, n_recent=0, n_sink=0)
-    qs, ks, vs = [], [], []
+    qs, ks, vs, regs = [], [], [], []
     lengths_fresh = torch.full((w.batch,), I, dtype=torch.int64, device=device)
     for _ in range(w.n_layers):
-        q, kf, vf = _layer(fresh_w, g, device, I, lengths_fresh, region_lo_offset=0)
+        q, kf, vf, reg = _layer(fresh_w, g, device, I, lengths_fresh, region_lo_offset=0)
         qs.append(q)
         ks.append(kf)
         vs.append(vf)
+        regs.append((reg[0] + Kb, reg[1], reg[2]))  # slots of the fresh part
     q = torch.stack(qs)
     k = torch.cat([k_out, torch.stack(ks)], dim=3).contiguous()
     v = torch.cat([v_out, torch.stack(vs)], dim=3).contiguous()
@@ -221,7 +232,8 @@ def next_event(w: Workload, prev: Inputs, k_out, v_out, credit_out, n_kept, even
     pad = torch.zeros((w.batch,), dtype=torch.int32, device=device)
     n_carry = torch.full((w.batch,), Kb, dtype=torch.int32, device=device)
     lengths = torch.full((w.batch,), T, dtype=torch.int64, device=device)
-    return Inputs(w, T, q, k, v, credit, pad, n_carry, lengths)
+    inp = Inputs(w, T, q, k, v, credit, pad, n_carry, lengths)
+    return (inp, _stack_regions(regs)) if return_regions else inp
 
 
 # ---- unit-major views (for the oracle, which works on compact [U, ...]) --------
