@@ -89,7 +89,7 @@ int cuda_fail(kvc_handle* h, cudaError_t e, const char* where) {
 
 const char* const kKernelNames[kvc::kNumKernels] = {
     "usage_pass1_rowstats_tcgen05", "usage_pass2_colsum_tcgen05", "mass_pool_ema",
-    "segment_quota", "select_topk", "gather_compact"};
+    "segment_quota", "select_topk", "gather_compact", "refresh_trigger"};
 
 cudaEvent_t prof_event(kvc_handle* h) {
   auto& P = h->prof;
@@ -422,6 +422,23 @@ int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
   KVC_REQUIRE_PTR(credit_out);
   return run_compact(h, k, v, credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out,
                      static_cast<cudaStream_t>(stream));
+}
+
+int kvc_refresh_decision(kvc_handle* h, const uint16_t* q, float* q_ref, float threshold,
+                         int32_t* flag, float* sim, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  if (!(threshold >= -1.f && threshold <= 1.f))
+    return fail(h, KVC_ERR_ARG, "threshold must lie in [-1, 1]");
+  KVC_REQUIRE_PTR(q);
+  KVC_REQUIRE_PTR(q_ref);
+  KVC_REQUIRE_PTR(flag);
+  KVC_REQUIRE_PTR(sim);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t b = mark_begin(h, s);
+  cudaError_t e = kvc::launch_refresh(h, q, q_ref, threshold, flag, sim, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "refresh trigger");
+  mark_end(h, kvc::kKernelRefresh, b, s);
+  return KVC_OK;
 }
 
 int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_t* v,

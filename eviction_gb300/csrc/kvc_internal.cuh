@@ -48,6 +48,7 @@ enum KernelId {
   kKernelSegmentQuota,
   kKernelSelect,
   kKernelCompact,
+  kKernelRefresh,
   kNumKernels
 };
 
@@ -115,6 +116,9 @@ cudaError_t launch_compact(const kvc_handle* h, const uint16_t* k,
                            const int32_t* kept_idx, const int32_t* n_kept,
                            uint16_t* k_out, uint16_t* v_out,
                            float* credit_out, cudaStream_t s);
+
+cudaError_t launch_refresh(const kvc_handle* h, const uint16_t* q, float* q_ref,
+                           float threshold, int32_t* flag, float* sim, cudaStream_t s);
 
 inline int s_max_of(const kvc_config& c, int T) {
   int s = T / c.seg_min;

@@ -19,7 +19,7 @@ _LIB_PATH = os.path.join(HERE, "libkvc.so")
 ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_sizes",
                 "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
                 "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
-                "kvc_profile_read", "kvc_mass_noalloc")
+                "kvc_profile_read", "kvc_mass_noalloc", "kvc_refresh_decision")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -134,6 +134,7 @@ def load_library():
     L.kvc_profile_read.argtypes = [_P, ctypes.POINTER(_KernelTime), _I, ctypes.POINTER(_I), _I]
     L.kvc_mass_noalloc.argtypes = [ctypes.POINTER(_CConfig), _P, _P, _I, _P, _P, _P, _P, _P, _P,
                                    _P, _P]
+    L.kvc_refresh_decision.argtypes = [_P, _P, _P, ctypes.c_float, _P, _P, _P]
     L.kvc_status_string.argtypes = [_I]
     L.kvc_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -268,6 +269,16 @@ class Handle:
             _dev(kept_idx, torch.int32, "kept_idx"), _dev(n_kept, torch.int32, "n_kept"),
             _stream_ptr(stream))
         self._check(rc, "kvc_event")
+
+    def refresh_decision(self, q, q_ref, threshold, flag, sim, stream=None):
+        """kvc_refresh_decision: q [L,B,H*G,d] bf16 (the current token), q_ref
+        [L,B,d] fp32 in/out, flag [L,B] int32 out, sim [L,B] fp32 out."""
+        import torch
+        rc = load_library().kvc_refresh_decision(
+            self._h, _dev(q, torch.bfloat16, "q"), _dev(q_ref, torch.float32, "q_ref"),
+            ctypes.c_float(threshold), _dev(flag, torch.int32, "flag"),
+            _dev(sim, torch.float32, "sim"), _stream_ptr(stream))
+        self._check(rc, "kvc_refresh_decision")
 
     def device_status(self, stream=None) -> int:
         bits = ctypes.c_uint32(0)

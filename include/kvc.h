@@ -166,6 +166,23 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
               uint16_t* k_out, uint16_t* v_out, float* credit_out,
               int32_t* kept_idx, int32_t* n_kept, void* stream);
 
+/* Query-similarity refresh trigger ("RefreshKV: Updating Small KV Cache During
+ * Long-form Generation", dynamic scheduling): for every (layer, sequence), the
+ * cosine similarity between the current decode token's query averaged over the
+ * H*G query heads and the reference query of that layer's last full step;
+ * below `threshold` a full (refresh) step is decided and the reference becomes
+ * the current averaged query.  A zero reference (none yet) or a zero query
+ * decides a refresh.  Called by the runtime every S-th decode step.
+ *   q      [L][B][H*G][d] bf16: the current token's queries (device);
+ *   q_ref  [L][B][d] fp32, in/out: reference queries, zero before any full step;
+ *   flag   [L][B] int32 out: 1 = take a full step / refresh, 0 = keep decoding
+ *          from the compressed cache;
+ *   sim    [L][B] fp32 out: the cosine (-2 where it is undefined).
+ * threshold in [-1, 1], else KVC_ERR_ARG.  Device pointers, 16-byte aligned,
+ * caller-owned; asynchronous on `stream`; no allocation. */
+int kvc_refresh_decision(kvc_handle* h, const uint16_t* q, float* q_ref, float threshold,
+                         int32_t* flag, float* sim, void* stream);
+
 /* ---- tracing -------------------------------------------------------------
  * While enabled, every entry point records a CUDA event on its stream after
  * each kernel it launches (and one before the first), so that the time of each

@@ -117,6 +117,7 @@ def _declare(L):
     L.kvc_ref_segment_quota.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P]
     L.kvc_ref_select.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     L.kvc_ref_compact.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
+    L.kvc_ref_refresh_decision.argtypes = [_I, _I, _I, _P, _P, ctypes.c_double, _P, _P]
 
 
 def _ptr(a: np.ndarray):
@@ -308,3 +309,17 @@ def event(p: RefParams, q_bits, k_bits, v_bits, credit_in, pad, n_carry):
     ko, vo, co = compact(p, k_bits, v_bits, c, kept, nk)
     return dict(mass=m, score=s, credit_post=c, seg_start=st, seg_len=ln, quota=qu, n_seg=ns,
                 kept_idx=kept, n_kept=nk, k_out=ko, v_out=vo, credit_out=co)
+
+
+def refresh_decision(q_bits, q_ref, threshold):
+    """RefreshKV query-similarity trigger for LB (layer, sequence) rows.
+    q_bits [LB, Hq, d] uint16, q_ref [LB, d] (copied; the updated copy is
+    returned).  Returns (flag [LB] int32, sim [LB] fp64, q_ref_new [LB, d])."""
+    q_bits = _c(q_bits, np.uint16)
+    LB, Hq, d = q_bits.shape
+    ref = np.array(q_ref, dtype=np.float64, copy=True, order="C").reshape(LB, d)
+    flag = np.zeros(LB, np.int32)
+    sim = np.zeros(LB, np.float64)
+    lib().kvc_ref_refresh_decision(LB, Hq, d, _ptr(q_bits), _ptr(ref), float(threshold),
+                                   _ptr(flag), _ptr(sim))
+    return flag, sim, ref

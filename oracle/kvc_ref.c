@@ -730,3 +730,46 @@ int kvc_ref_compact(const kvc_ref_config* cfg, int U, int T, const uint16_t* k,
   }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Query-similarity refresh trigger                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [RefreshKV] "Deciding when to decode with full cache" / "Dynamic scheduling":
+ * every S-th decode step, for each layer, the cosine similarity between the
+ * query of the current token averaged over all query heads and the averaged
+ * query of the layer's most recent full-attention step decides: above the
+ * threshold s the partial cache is used, otherwise the layer takes a full
+ * step (and that step's averaged query becomes the new reference).
+ * Readings:
+ *  [R] one decision per (layer, sequence of the batch);
+ *  [R] a zero reference (no full step yet) or a zero current query (cosine
+ *      undefined) decides a refresh; sim = -2 marks the undefined cosine;
+ *  [R] "below the threshold" is strict: sim < s refreshes.
+ */
+void kvc_ref_refresh_decision(int LB, int Hq, int d, const uint16_t* q, double* q_ref,
+                              double threshold, int32_t* flag, double* sim) {
+  double* mean = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int r = 0; r < LB; ++r) {
+    for (int i = 0; i < d; ++i) mean[i] = 0.0;
+    for (int h = 0; h < Hq; ++h)
+      for (int i = 0; i < d; ++i)
+        mean[i] += bf16_to_double(q[((size_t)r * Hq + h) * d + i]);
+    for (int i = 0; i < d; ++i) mean[i] /= (double)Hq;
+    double dot = 0.0, nq = 0.0, nr = 0.0;
+    double* ref = q_ref + (size_t)r * d;
+    for (int i = 0; i < d; ++i) {
+      dot += mean[i] * ref[i];
+      nq += mean[i] * mean[i];
+      nr += ref[i] * ref[i];
+    }
+    const int defined = nq > 0.0 && nr > 0.0;
+    const double c = defined ? dot / (sqrt(nq) * sqrt(nr)) : -2.0;
+    sim[r] = c;
+    flag[r] = (!defined || c < threshold) ? 1 : 0;
+    if (flag[r])
+      for (int i = 0; i < d; ++i) ref[i] = mean[i];
+  }
+  free(mean);
+}

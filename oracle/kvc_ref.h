@@ -152,6 +152,14 @@ int kvc_ref_compact(const kvc_ref_config* cfg, int U, int T, const uint16_t* k,
                     const int32_t* kept_idx, const int32_t* n_kept,
                     uint16_t* k_out, uint16_t* v_out, float* credit_out);
 
+/* [RefreshKV] query-similarity trigger, per (layer, sequence) row of LB rows:
+ * the current token's query averaged over the Hq query heads (q: [LB][Hq][d]
+ * bf16 bits) against the reference query of the last full step (q_ref: [LB][d],
+ * updated where a refresh is decided).  flag[r] = 1 where the cosine is below
+ * `threshold` (or undefined), else 0; sim[r] = the cosine (-2 when undefined). */
+void kvc_ref_refresh_decision(int LB, int Hq, int d, const uint16_t* q, double* q_ref,
+                              double threshold, int32_t* flag, double* sim);
+
 #ifdef __cplusplus
 }
 #endif
