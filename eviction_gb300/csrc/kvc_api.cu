@@ -89,7 +89,7 @@ int cuda_fail(kvc_handle* h, cudaError_t e, const char* where) {
 
 const char* const kKernelNames[kvc::kNumKernels] = {
     "usage_pass1_rowstats_tcgen05", "usage_pass2_colsum_tcgen05", "mass_pool_ema",
-    "segment_quota", "select_topk", "gather_compact", "refresh_trigger"};
+    "segment_quota", "select_topk", "gather_compact", "refresh_trigger", "compact_paged"};
 
 cudaEvent_t prof_event(kvc_handle* h) {
   auto& P = h->prof;
@@ -422,6 +422,43 @@ int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
   KVC_REQUIRE_PTR(credit_out);
   return run_compact(h, k, v, credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out,
                      static_cast<cudaStream_t>(stream));
+}
+
+int kvc_compact_paged(kvc_handle* h, uint16_t* k_pool, uint16_t* v_pool, int n_blocks,
+                      int block_size, int max_blocks, const int32_t* seq_len,
+                      const int32_t* pad, const int32_t* kept_idx, const int32_t* n_kept,
+                      const float* credit_post, int T, float* credit_out,
+                      const int32_t* table_old, int32_t* table_new, int32_t* free_list,
+                      int32_t* free_top, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  if (n_blocks < 1 || block_size < 1 || max_blocks < 1)
+    return fail(h, KVC_ERR_ARG, "n_blocks, block_size and max_blocks must be >= 1");
+  if ((static_cast<int64_t>(block_size) * h->dims.d * 2) % 16 != 0)
+    return fail(h, KVC_ERR_ALIGN, "block rows must be 16-byte multiples");
+  KVC_REQUIRE_PTR(k_pool);
+  KVC_REQUIRE_PTR(v_pool);
+  KVC_REQUIRE_PTR(seq_len);
+  KVC_REQUIRE_PTR(pad);
+  KVC_REQUIRE_PTR(kept_idx);
+  KVC_REQUIRE_PTR(n_kept);
+  KVC_REQUIRE_PTR(credit_post);
+  KVC_REQUIRE_PTR(credit_out);
+  KVC_REQUIRE_PTR(table_old);
+  KVC_REQUIRE_PTR(table_new);
+  KVC_REQUIRE_PTR(free_list);
+  if (!free_top || (reinterpret_cast<uintptr_t>(free_top) & 3u))
+    return fail(h, KVC_ERR_ALIGN, "free_top must be a 4-byte aligned device int32");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kvc::PagedArgs a{k_pool,   v_pool,      n_blocks,   block_size, max_blocks, T,
+                   seq_len,  pad,         kept_idx,   n_kept,     credit_post, credit_out,
+                   table_old, table_new,  free_list,  free_top};
+  cudaEvent_t b = mark_begin(h, s);
+  cudaError_t e = kvc::launch_compact_paged(h, a, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "paged compaction");
+  mark_end(h, kvc::kKernelCompactPaged, b, s);
+  return KVC_OK;
 }
 
 int kvc_refresh_decision(kvc_handle* h, const uint16_t* q, float* q_ref, float threshold,

@@ -28,7 +28,8 @@ struct Workspace {
   int32_t* seg_len = nullptr;
   int32_t* quota = nullptr;
   int32_t* n_seg = nullptr;     // [U]
-  uint32_t* status = nullptr;   // device status bits
+  uint32_t* status = nullptr;   // device status bits; status[1] = the error word of
+                                // the running paged compaction
   void* base = nullptr;         // single allocation
   size_t bytes = 0;
 };
@@ -49,6 +50,7 @@ enum KernelId {
   kKernelSelect,
   kKernelCompact,
   kKernelRefresh,
+  kKernelCompactPaged,
   kNumKernels
 };
 
@@ -116,6 +118,26 @@ cudaError_t launch_compact(const kvc_handle* h, const uint16_t* k,
                            const int32_t* kept_idx, const int32_t* n_kept,
                            uint16_t* k_out, uint16_t* v_out,
                            float* credit_out, cudaStream_t s);
+
+struct PagedArgs {
+  uint16_t* k_pool;
+  uint16_t* v_pool;
+  int n_blocks, block_size, max_blocks, T;
+  const int32_t* seq_len;
+  const int32_t* pad;
+  const int32_t* kept_idx;
+  const int32_t* n_kept;
+  const float* credit_post;
+  float* credit_out;
+  const int32_t* table_old;
+  int32_t* table_new;
+  int32_t* free_list;
+  int32_t* free_top;
+};
+
+// Paged compaction (validate, allocate, copy, free); errors land in the word
+// after the status word and are OR-ed into the status at the end.
+cudaError_t launch_compact_paged(const kvc_handle* h, const PagedArgs& a, cudaStream_t s);
 
 cudaError_t launch_refresh(const kvc_handle* h, const uint16_t* q, float* q_ref,
                            float threshold, int32_t* flag, float* sim, cudaStream_t s);

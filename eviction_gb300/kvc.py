@@ -19,7 +19,8 @@ _LIB_PATH = os.path.join(HERE, "libkvc.so")
 ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_sizes",
                 "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
                 "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
-                "kvc_profile_read", "kvc_mass_noalloc", "kvc_refresh_decision")
+                "kvc_profile_read", "kvc_mass_noalloc", "kvc_refresh_decision",
+                "kvc_compact_paged")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -135,6 +136,8 @@ def load_library():
     L.kvc_mass_noalloc.argtypes = [ctypes.POINTER(_CConfig), _P, _P, _I, _P, _P, _P, _P, _P, _P,
                                    _P, _P]
     L.kvc_refresh_decision.argtypes = [_P, _P, _P, ctypes.c_float, _P, _P, _P]
+    L.kvc_compact_paged.argtypes = [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P,
+                                    _P, _P, _P]
     L.kvc_status_string.argtypes = [_I]
     L.kvc_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -279,6 +282,26 @@ class Handle:
             ctypes.c_float(threshold), _dev(flag, torch.int32, "flag"),
             _dev(sim, torch.float32, "sim"), _stream_ptr(stream))
         self._check(rc, "kvc_refresh_decision")
+
+    def compact_paged(self, k_pool, v_pool, block_size, seq_len, pad, kept_idx, n_kept,
+                      credit_post, T, credit_out, table_old, table_new, free_list, free_top,
+                      stream=None):
+        """kvc_compact_paged: pools [L, n_blocks, H, bs, d] bf16 (in/out), tables
+        [B, max_blocks] int32, free_list [n_blocks] int32 and free_top [1] int32
+        (in/out), credit_post [L,B,H,T] -> credit_out [L,B,H,budget]."""
+        import torch
+        n_blocks = k_pool.shape[1]
+        max_blocks = table_old.shape[1]
+        rc = load_library().kvc_compact_paged(
+            self._h, _dev(k_pool, torch.bfloat16, "k_pool"), _dev(v_pool, torch.bfloat16, "v_pool"),
+            n_blocks, block_size, max_blocks, _dev(seq_len, torch.int32, "seq_len"),
+            _dev(pad, torch.int32, "pad"), _dev(kept_idx, torch.int32, "kept_idx"),
+            _dev(n_kept, torch.int32, "n_kept"), _dev(credit_post, torch.float32, "credit_post"), T,
+            _dev(credit_out, torch.float32, "credit_out"),
+            _dev(table_old, torch.int32, "table_old"), _dev(table_new, torch.int32, "table_new"),
+            _dev(free_list, torch.int32, "free_list"), _dev(free_top, torch.int32, "free_top"),
+            _stream_ptr(stream))
+        self._check(rc, "kvc_compact_paged")
 
     def device_status(self, stream=None) -> int:
         bits = ctypes.c_uint32(0)

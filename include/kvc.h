@@ -77,7 +77,13 @@ extern "C" {
 #define KVC_STATUS_WAIT_TIMEOUT 0x1u /* an mbarrier wait hit its bound; the
                                         affected outputs are unspecified     */
 #define KVC_STATUS_BAD_INDEX 0x2u    /* kvc_compact got a kept index outside
-                                        [0, T): that row was written as zeros */
+                                        [0, T): that row was written as zeros;
+                                        kvc_compact_paged: an index, block or
+                                        free-stack entry out of range (nothing
+                                        was changed)                          */
+#define KVC_STATUS_POOL_EXHAUSTED 0x4u /* kvc_compact_paged: the free stack
+                                        held fewer blocks than the compacted
+                                        caches need (nothing was changed)     */
 
 /* ---- configuration ------------------------------------------------------ */
 typedef struct {
@@ -165,6 +171,42 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
               const int32_t* n_carry, const float* credit_in,
               uint16_t* k_out, uint16_t* v_out, float* credit_out,
               int32_t* kept_idx, int32_t* n_kept, void* stream);
+
+/* Step 6 into a paged KV pool ("Adaptive Mass-Segmented KV Compression for
+ * Long-Form Reasoning", Appendix E): new blocks are taken from a free stack,
+ * each head's kept rows are copied from their original positions into the
+ * new physical slots, the sequence's new block table is written and its old
+ * blocks are pushed back onto the stack.
+ *   k_pool, v_pool  [L][n_blocks][H][block_size][d] bf16, in/out: logical
+ *                   token t of sequence b, layer l, head h is row t % bs of
+ *                   block table[b][t / bs] (one table per sequence, shared by
+ *                   all layers);
+ *   seq_len [B]     tokens per sequence before the event;
+ *   pad [B]         as for the other entry points: kept_idx holds dense slots,
+ *                   the logical position is slot - pad[b];
+ *   kept_idx, n_kept  from kvc_select / kvc_event ([L][B][H][budget], [L][B][H];
+ *                   n_kept must be the same for every layer and head of a
+ *                   sequence, as the method makes it);
+ *   credit_post [L][B][H][T] -> credit_out [L][B][H][budget] (dense, as in
+ *                   kvc_compact; slots past n_kept are 0);
+ *   table_old [B][max_blocks] in, table_new [B][max_blocks] out (-1 past the
+ *                   ceil(n_kept / bs) new blocks);
+ *   free_list [n_blocks] and *free_top (device int32), in/out: entries
+ *                   [0, *free_top) are free; sequence b takes the next
+ *                   ceil(n_kept_b / bs) entries below the top in sequence
+ *                   order (deterministic), and its ceil(seq_len_b / bs) old
+ *                   blocks are pushed back afterwards in sequence order.
+ * block_size >= 1, n_blocks >= 1, max_blocks >= 1, T as for kvc_compact.  On a
+ * device-side failure nothing is changed and KVC_STATUS_POOL_EXHAUSTED or
+ * KVC_STATUS_BAD_INDEX is set (kvc_get_device_status).  The pools must not be
+ * used by other work on other streams during the call; asynchronous on
+ * `stream`; no allocation. */
+int kvc_compact_paged(kvc_handle* h, uint16_t* k_pool, uint16_t* v_pool, int n_blocks,
+                      int block_size, int max_blocks, const int32_t* seq_len,
+                      const int32_t* pad, const int32_t* kept_idx, const int32_t* n_kept,
+                      const float* credit_post, int T, float* credit_out,
+                      const int32_t* table_old, int32_t* table_new, int32_t* free_list,
+                      int32_t* free_top, void* stream);
 
 /* Query-similarity refresh trigger ("RefreshKV: Updating Small KV Cache During
  * Long-form Generation", dynamic scheduling): for every (layer, sequence), the

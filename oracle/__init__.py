@@ -118,6 +118,8 @@ def _declare(L):
     L.kvc_ref_select.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     L.kvc_ref_compact.argtypes = [_P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     L.kvc_ref_refresh_decision.argtypes = [_I, _I, _I, _P, _P, ctypes.c_double, _P, _P]
+    L.kvc_ref_compact_paged.argtypes = [_I] * 8 + [_P] * 10
+    L.kvc_ref_compact_paged.restype = _I
 
 
 def _ptr(a: np.ndarray):
@@ -323,3 +325,29 @@ def refresh_decision(q_bits, q_ref, threshold):
     lib().kvc_ref_refresh_decision(LB, Hq, d, _ptr(q_bits), _ptr(ref), float(threshold),
                                    _ptr(flag), _ptr(sim))
     return flag, sim, ref
+
+
+def compact_paged(k_pool, v_pool, seq_len, pad, kept_idx, n_kept, table_old, free_list,
+                  free_top, block_size):
+    """Paged compaction on copies of the pools and the free list.  k_pool, v_pool
+    [L, n_blocks, H, bs, d] uint16; kept_idx [L, B, H, budget]; n_kept [L, B, H];
+    table_old [B, max_blocks].  Returns (rc, k_pool, v_pool, table_new,
+    free_list, free_top)."""
+    kp = np.array(k_pool, dtype=np.uint16, copy=True, order="C")
+    vp = np.array(v_pool, dtype=np.uint16, copy=True, order="C")
+    L, n_blocks, H, bs, d = kp.shape
+    assert bs == block_size
+    kept = _c(kept_idx, np.int32)
+    budget = kept.shape[-1]
+    B = kept.shape[1]
+    told = _c(table_old, np.int32)
+    max_blocks = told.shape[1]
+    tnew = np.full((B, max_blocks), -1, np.int32)
+    fl = np.array(free_list, dtype=np.int32, copy=True, order="C")
+    top = np.array([free_top], np.int32)
+    rc = lib().kvc_ref_compact_paged(L, B, H, d, bs, n_blocks, max_blocks, budget, _ptr(kp),
+                                     _ptr(vp), _ptr(_c(seq_len, np.int32)),
+                                     _ptr(_c(pad, np.int32)), _ptr(kept),
+                                     _ptr(_c(n_kept, np.int32)), _ptr(told), _ptr(tnew),
+                                     _ptr(fl), _ptr(top))
+    return rc, kp, vp, tnew, fl, int(top[0])

@@ -773,3 +773,88 @@ void kvc_ref_refresh_decision(int LB, int Hq, int d, const uint16_t* q, double* 
   }
   free(mean);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Paged compaction                                                           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [AMS] Appendix E: the selection is separated from the paged storage layout.
+ * The method outputs the kept indices per head; the runtime allocates new
+ * blocks, copies each head's KV from its original positions into the new
+ * physical slots, replaces the request's block table and frees the old
+ * blocks.  The same compacted slot may hold different original positions in
+ * different heads.
+ * Readings (the page gives the steps, not the data structures):
+ *  [R] pools [L][n_blocks][H][bs][d]; one block table per sequence, shared by
+ *      all layers (every layer and head of a sequence keeps the same count);
+ *  [R] the free blocks form a stack; allocation for all sequences happens
+ *      before any copy (old and new blocks coexist during the copy), in
+ *      sequence order from the top of the stack; the old blocks are pushed
+ *      back afterwards, in sequence order;
+ *  [R] kept slot j of head h goes to block table_new[b][j / bs], row j % bs.
+ */
+int kvc_ref_compact_paged(int L, int B, int H, int d, int bs, int n_blocks, int max_blocks,
+                          int budget, uint16_t* k_pool, uint16_t* v_pool,
+                          const int32_t* seq_len, const int32_t* pad,
+                          const int32_t* kept_idx, const int32_t* n_kept,
+                          const int32_t* table_old, int32_t* table_new,
+                          int32_t* free_list, int32_t* free_top) {
+  /* blocks needed after compaction, per sequence (same count in every head) */
+  int64_t need_total = 0;
+  for (int b = 0; b < B; ++b) {
+    const int nk = n_kept[(size_t)b * H];  /* layer 0, head 0 */
+    if (nk < 0 || nk > budget || (nk + bs - 1) / bs > max_blocks) return -1;
+    for (int l = 0; l < L; ++l)
+      for (int h = 0; h < H; ++h)
+        if (n_kept[((size_t)l * B + b) * H + h] != nk) return -1;
+    need_total += (nk + bs - 1) / bs;
+  }
+  if (need_total > *free_top) return -1;
+  /* check every source position before changing anything */
+  for (int l = 0; l < L; ++l)
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h) {
+        const size_t u = ((size_t)l * B + b) * H + h;
+        for (int j = 0; j < n_kept[u]; ++j) {
+          const int t = kept_idx[u * budget + j] - pad[b];
+          if (t < 0 || t >= seq_len[b]) return -1;
+          const int blk = table_old[(size_t)b * max_blocks + t / bs];
+          if (blk < 0 || blk >= n_blocks) return -1;
+        }
+      }
+  /* allocate: sequence b takes the next blocks from the top of the stack */
+  int64_t pos = *free_top - need_total;
+  for (int b = 0; b < B; ++b) {
+    const int nk = n_kept[(size_t)b * H];
+    const int nb = (nk + bs - 1) / bs;
+    for (int i = 0; i < max_blocks; ++i)
+      table_new[(size_t)b * max_blocks + i] = i < nb ? free_list[pos + i] : -1;
+    pos += nb;
+  }
+  *free_top -= (int32_t)need_total;
+  /* copy each head's kept rows into the new blocks */
+  const size_t row = (size_t)d;
+  for (int l = 0; l < L; ++l)
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < H; ++h) {
+        const size_t u = ((size_t)l * B + b) * H + h;
+        for (int j = 0; j < n_kept[u]; ++j) {
+          const int t = kept_idx[u * budget + j] - pad[b];
+          const int src_blk = table_old[(size_t)b * max_blocks + t / bs];
+          const int dst_blk = table_new[(size_t)b * max_blocks + j / bs];
+          const size_t src = ((((size_t)l * n_blocks + src_blk) * H + h) * bs + t % bs) * row;
+          const size_t dst = ((((size_t)l * n_blocks + dst_blk) * H + h) * bs + j % bs) * row;
+          for (int i = 0; i < d; ++i) {
+            k_pool[dst + i] = k_pool[src + i];
+            v_pool[dst + i] = v_pool[src + i];
+          }
+        }
+      }
+  /* free the old blocks, in sequence order */
+  for (int b = 0; b < B; ++b) {
+    const int nb_old = (seq_len[b] + bs - 1) / bs;
+    for (int i = 0; i < nb_old; ++i) free_list[(*free_top)++] = table_old[(size_t)b * max_blocks + i];
+  }
+  return 0;
+}

@@ -152,6 +152,25 @@ int kvc_ref_compact(const kvc_ref_config* cfg, int U, int T, const uint16_t* k,
                     const int32_t* kept_idx, const int32_t* n_kept,
                     uint16_t* k_out, uint16_t* v_out, float* credit_out);
 
+/* [AMS] Appendix E, paged layout: per-head compaction into newly allocated
+ * blocks.  Pools k_pool, v_pool: [L][n_blocks][H][bs][d] bf16 bits (in/out);
+ * block tables [B][max_blocks] shared by all layers (logical token t of
+ * sequence b lives in block table[b][t / bs], row t % bs); seq_len [B] tokens
+ * before the event; pad [B] converts the dense slots of kept_idx
+ * ([L][B][H][budget], n_kept [L][B][H]) to logical positions (t = slot - pad).
+ * free_list [n_blocks] with *free_top entries free, used as a stack: sequence
+ * b takes ceil(n_kept_b / bs) blocks in sequence order from the top, the copy
+ * follows, then the ceil(seq_len_b / bs) old blocks are pushed back in
+ * sequence order.  table_new [B][max_blocks] gets the new blocks (-1 past
+ * them).  Returns 0, or -1 (nothing changed) if the pool cannot supply the
+ * blocks or an index is out of range. */
+int kvc_ref_compact_paged(int L, int B, int H, int d, int bs, int n_blocks, int max_blocks,
+                          int budget, uint16_t* k_pool, uint16_t* v_pool,
+                          const int32_t* seq_len, const int32_t* pad,
+                          const int32_t* kept_idx, const int32_t* n_kept,
+                          const int32_t* table_old, int32_t* table_new,
+                          int32_t* free_list, int32_t* free_top);
+
 /* [RefreshKV] query-similarity trigger, per (layer, sequence) row of LB rows:
  * the current token's query averaged over the Hq query heads (q: [LB][Hq][d]
  * bf16 bits) against the reference query of the last full step (q_ref: [LB][d],
