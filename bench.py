@@ -40,6 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 from eviction_gb300.kvc import ABLATIONS  # noqa: E402  (the pages' ablations as switches)
 
 KERNEL_SOURCES = {
+    "compact_paged": "paged.cu",
+    "refresh_trigger": "refresh.cu",
     "usage_pass1_rowstats_tcgen05": "attn_usage.cu",
     "usage_pass2_colsum_tcgen05": "attn_usage.cu",
     "mass_pool_ema": "mass_post.cu",
@@ -62,6 +64,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged", action="store_true",
+                    help="compact into a paged KV pool (block size 16) instead of dense caches")
     ap.add_argument("--ablation", choices=sorted(ABLATIONS), default="none",
                     help="time one of the method's ablations (the pages' ablation table)")
     return ap.parse_args()
@@ -98,6 +102,8 @@ def unit_work(w, T_valid, T):
         "select_topk": ("hbm", 0.0, 4.0 * T + 4.0 * Kb),
         # kept K and V rows read, written; credit read/written; indices read
         "gather_compact": ("hbm", 0.0, 8.0 * Kb * d + 12.0 * Kb),
+        # the same rows and credit moved into pool blocks; plus indices validated
+        "compact_paged": ("hbm", 0.0, 8.0 * Kb * d + 16.0 * Kb),
     }
     return flops, ev_bytes, per_kernel
 
@@ -282,7 +288,7 @@ def run_reference(args, w):
     print(json.dumps(line))
 
 
-def workload_config(w, T, ablation="none"):
+def workload_config(w, T, ablation="none", paged=False):
     cfg = {"workload": (f"{w.name}: {w.n_layers} layers x batch {w.batch} x {w.n_kv_heads} KV heads"
                          f" (GQA {w.group}), d {w.head_dim}, {T} slots -> budget {w.budget}, "
                          f"window {w.window}" + (", event 2 (credit carried, 512 fresh slots)"
@@ -292,6 +298,8 @@ def workload_config(w, T, ablation="none"):
             "l2": "inputs larger than L2 (no flush needed)"}
     if ablation != "none":
         cfg["ablation"] = f"{ablation}: {ABLATIONS[ablation]}"
+    if paged:
+        cfg["paged"] = "compaction into a paged pool, block size 16 (stack and table restored per step)"
     return cfg
 
 
@@ -337,6 +345,57 @@ def run_ours(args, w):
     def step():
         h.event(inp.q, inp.k, inp.v, T, inp.pad, inp.n_carry, inp.credit, out["k_out"],
                 out["v_out"], out["credit_out"], out["kept_idx"], out["n_kept"])
+
+    if args.paged:
+        args.no_e2e = True  # the host round trip is timed for the dense path only
+        # the same cache in a paged pool (block size 16, a random block table);
+        # one step = steps 1-5 through the stage entry points, then the paged
+        # compaction; the stack and table are restored before each step
+        bs = 16
+        lens = (T - inp.pad.long()).tolist()
+        max_blocks = (T + bs - 1) // bs
+        n_old = sum((n + bs - 1) // bs for n in lens)
+        n_new = w.batch * ((w.budget + bs - 1) // bs)
+        n_blocks = n_old + n_new
+        perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(0)).to(torch.int32)
+        table0 = torch.full((w.batch, max_blocks), -1, dtype=torch.int32)
+        at = 0
+        for b, n in enumerate(lens):
+            nb = (n + bs - 1) // bs
+            table0[b, :nb] = perm[at:at + nb]
+            at += nb
+        free0 = torch.zeros(n_blocks, dtype=torch.int32)
+        free0[:n_new] = perm[n_old:]
+        table0, free0 = table0.to(dev), free0.to(dev)
+        top0 = torch.tensor([n_new], dtype=torch.int32, device=dev)
+        L_, H_, d_ = w.n_layers, w.n_kv_heads, w.head_dim
+        k_pool = torch.zeros((L_, n_blocks, H_, bs, d_), dtype=torch.bfloat16, device=dev)
+        v_pool = torch.zeros_like(k_pool)
+        t_idx = torch.arange(T, device=dev)
+        for b, n in enumerate(lens):
+            pb = T - n
+            pos = t_idx[:n]
+            blk = table0[b, pos // bs].long()
+            k_pool[:, blk, :, pos % bs] = inp.k[:, b, :, pb:].permute(2, 0, 1, 3)
+            v_pool[:, blk, :, pos % bs] = inp.v[:, b, :, pb:].permute(2, 0, 1, 3)
+        seq_len = torch.tensor(lens, dtype=torch.int32, device=dev)
+        stage = h.stage_buffers(T, dev)
+        table, free, top = table0.clone(), free0.clone(), top0.clone()
+        table_new = torch.empty_like(table0)
+
+        def step():  # noqa: F811
+            table.copy_(table0)
+            free.copy_(free0)
+            top.copy_(top0)
+            h.mass(inp.q, inp.k, T, inp.pad, inp.n_carry, inp.credit, stage["credit_post"],
+                   stage["mass"], stage["score"])
+            h.segment_quota(stage["mass"], T, inp.pad, stage["seg_start"], stage["seg_len"],
+                            stage["quota"], stage["n_seg"])
+            h.select(stage["score"], T, inp.pad, stage["seg_start"], stage["seg_len"],
+                     stage["quota"], stage["n_seg"], out["kept_idx"], out["n_kept"])
+            h.compact_paged(k_pool, v_pool, bs, seq_len, inp.pad, out["kept_idx"], out["n_kept"],
+                            stage["credit_post"], T, out["credit_out"], table, table_new, free,
+                            top)
 
     warm = max(3, args.warmup)
     try:
@@ -477,12 +536,14 @@ def run_ours(args, w):
                          f"same inputs, single-threaded C oracle (fp64); host copies included"}
 
     clocks = summarize_clocks(clock_rows, t_wall0, t_wall1)
-    launches = sum(r["launches"] for r in krows)
+    # kernels per traced entry (the paged compaction is four launches)
+    launches = sum(r["launches"] * (4 if r["name"] == "compact_paged" else 1) for r in krows)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w, T, args.ablation), parallelism=f"replicas x{world}"),
+        "config": dict(workload_config(w, T, args.ablation, args.paged),
+                       parallelism=f"replicas x{world}"),
         "roofline": roofline, "event_roofline": event_roofline,
         "kernels": [{k2: (round(v, 6) if isinstance(v, float) else v) for k2, v in r.items()}
                     for r in krows],
