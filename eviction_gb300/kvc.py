@@ -47,7 +47,8 @@ class _CConfig(ctypes.Structure):
                 ("q_min", ctypes.c_int), ("n_sink", ctypes.c_int), ("n_recent", ctypes.c_int),
                 ("lambda_", ctypes.c_float), ("beta", ctypes.c_float), ("eps", ctypes.c_float),
                 ("softmax_scale", ctypes.c_float), ("seg_fixed", ctypes.c_int),
-                ("quota_by_len", ctypes.c_int), ("global_topk", ctypes.c_int)]
+                ("quota_by_len", ctypes.c_int), ("global_topk", ctypes.c_int),
+                ("redundancy_sigma", ctypes.c_float)]
 
 
 # The ablations of the method's ablation table as Config keyword switches
@@ -87,13 +88,15 @@ class Config:
     seg_fixed: int = 0       # ablation: fixed-length segments (0 = mass cut points)
     quota_by_len: int = 0    # ablation: quotas by segment length instead of mass
     global_topk: int = 0     # ablation: one segment, per-head global top-k
+    redundancy_sigma: float = 0.0  # > 0: select on sigma*I - (1-sigma)*R (key redundancy)
 
     def c(self) -> _CConfig:
         return _CConfig(self.n_layers, self.batch, self.n_kv_heads, self.group, self.head_dim,
                         self.max_T, self.window, self.budget, self.avg_pool, self.max_pool,
                         self.delta, self.seg_min, self.seg_max, self.q_min, self.n_sink,
                         self.n_recent, self.lam, self.beta, self.eps, self.softmax_scale,
-                        self.seg_fixed, self.quota_by_len, self.global_topk)
+                        self.seg_fixed, self.quota_by_len, self.global_topk,
+                        self.redundancy_sigma)
 
     @property
     def units(self):

@@ -118,6 +118,11 @@ typedef struct {
                         segment mass (same minimums, rounding, correction)  */
   int global_topk;   /* 1: one segment over all valid slots, quota = budget:
                         per-head top-k on the score plus the must-keep set  */
+  /* Second base score ("SkipKV: ...", A2 token redundancy score, after R-KV):
+   * sigma in (0, 1] selects on sigma*I - (1-sigma)*R instead of the score
+   * (see kvc_redundancy_score); 0 = off.  Segments and quotas stay on the
+   * attention mass.                                                         */
+  float redundancy_sigma;
 } kvc_config;
 
 typedef struct kvc_handle kvc_handle;

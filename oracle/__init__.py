@@ -10,7 +10,8 @@ module only compiles it with gcc and marshals numpy arrays through ctypes.
 Sources: "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning"
 (Method, Key designs 1-4; the complete example), "RefreshKV: Updating Small KV
 Cache During Long-form Generation" (A2 max pooling; A6 kernel size 7) and
-"SkipKV: ..." (A2 token importance score, GQA mapping and mask).
+"SkipKV: ..." (A2 token importance score, GQA mapping and mask; A2 token
+redundancy score and the sigma mix of the final score).
 """
 from __future__ import annotations
 
@@ -51,6 +52,7 @@ class _Cfg(ctypes.Structure):
         ("lambda_", ctypes.c_float), ("beta", ctypes.c_float), ("eps", ctypes.c_float),
         ("softmax_scale", ctypes.c_float), ("seg_fixed", ctypes.c_int),
         ("quota_by_len", ctypes.c_int), ("global_topk", ctypes.c_int),
+        ("redundancy_sigma", ctypes.c_float),
     ]
 
 
@@ -76,12 +78,14 @@ class RefParams:
     seg_fixed: int = 0       # ablation: fixed-length segments
     quota_by_len: int = 0    # ablation: quotas by length
     global_topk: int = 0     # ablation: one segment per unit
+    redundancy_sigma: float = 0.0  # > 0: select on the redundancy-mixed score
 
     def c(self) -> _Cfg:
         return _Cfg(self.group, self.head_dim, self.window, self.budget, self.avg_pool,
                     self.max_pool, self.delta, self.seg_min, self.seg_max, self.q_min,
                     self.n_sink, self.n_recent, self.lam, self.beta, self.eps,
-                    self.softmax_scale, self.seg_fixed, self.quota_by_len, self.global_topk)
+                    self.softmax_scale, self.seg_fixed, self.quota_by_len, self.global_topk,
+                    self.redundancy_sigma)
 
 
 def lib():
@@ -120,6 +124,8 @@ def _declare(L):
     L.kvc_ref_refresh_decision.argtypes = [_I, _I, _I, _P, _P, ctypes.c_double, _P, _P]
     L.kvc_ref_compact_paged.argtypes = [_I] * 8 + [_P] * 10
     L.kvc_ref_compact_paged.restype = _I
+    L.kvc_ref_mean_cosine_rows.argtypes = [_P, _I, _I, _I, _P, _I, _P]
+    L.kvc_ref_redundancy_score.argtypes = [_P, _P, _I, _I, _I, ctypes.c_double, _P, _P, _P]
 
 
 def _ptr(a: np.ndarray):
@@ -303,14 +309,51 @@ def compact(p: RefParams, k_bits, v_bits, credit_post, kept_idx, n_kept):
     return ko, vo, co
 
 
+def mean_cosine_rows(k_bits, pad, rows):
+    """SkipKV token redundancy of single rows: k_bits [T, d] uint16 (one unit),
+    rows: absolute slots.  Returns r [len(rows)] fp64 (mean cosine to the other
+    valid keys)."""
+    k_bits = _c(k_bits, np.uint16)
+    T, d = k_bits.shape
+    rows = _c(rows, np.int32)
+    out = np.zeros(len(rows), np.float64)
+    lib().kvc_ref_mean_cosine_rows(_ptr(k_bits), T, d, int(pad), _ptr(rows), len(rows), _ptr(out))
+    return out
+
+
+def redundancy_score(k_bits, score, pad, sigma):
+    """SkipKV redundancy-mixed score for U units: k_bits [U, T, d] uint16, score
+    [U, T] f32, pad [U].  Returns (f, R, r), each [U, T] fp64: the final score,
+    the softmax-normalised redundancy and the mean cosine."""
+    k_bits = _c(k_bits, np.uint16)
+    U, T, d = k_bits.shape
+    score = _c(score, np.float32).reshape(U, T)
+    pad = np.asarray(pad, np.int64).reshape(U)
+    f = np.zeros((U, T))
+    R = np.zeros((U, T))
+    r = np.zeros((U, T))
+    for u in range(U):
+        lib().kvc_ref_redundancy_score(_ptr(k_bits[u]), _ptr(score[u]), T, d, int(pad[u]),
+                                       float(sigma), _ptr(r[u]), _ptr(R[u]), _ptr(f[u]))
+    return f, R, r
+
+
 def event(p: RefParams, q_bits, k_bits, v_bits, credit_in, pad, n_carry):
-    """The whole event, steps 1-6, for U units. Returns a dict of numpy arrays."""
+    """The whole event, steps 1-6, for U units. Returns a dict of numpy arrays.
+    With p.redundancy_sigma > 0 step 5 selects on the SkipKV redundancy-mixed
+    score (rounded to fp32, the score's own precision); "sel_score" holds it."""
     m, s, c = mass(p, q_bits, k_bits, credit_in, pad, n_carry)
     st, ln, qu, ns = segment_quota(p, m, pad)
-    kept, nk = select(p, s, pad, st, ln, qu, ns)
+    sel = s
+    extra = {}
+    if p.redundancy_sigma > 0:
+        f, R, r = redundancy_score(k_bits, s, pad, p.redundancy_sigma)
+        sel = f.astype(np.float32)
+        extra = dict(sel_score=sel, redundancy=R, mean_cos=r)
+    kept, nk = select(p, sel, pad, st, ln, qu, ns)
     ko, vo, co = compact(p, k_bits, v_bits, c, kept, nk)
     return dict(mass=m, score=s, credit_post=c, seg_start=st, seg_len=ln, quota=qu, n_seg=ns,
-                kept_idx=kept, n_kept=nk, k_out=ko, v_out=vo, credit_out=co)
+                kept_idx=kept, n_kept=nk, k_out=ko, v_out=vo, credit_out=co, **extra)
 
 
 def refresh_decision(q_bits, q_ref, threshold):

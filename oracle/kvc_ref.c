@@ -576,6 +576,100 @@ int kvc_ref_select_unit(const float* score, int T, int pad,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Second base score: key redundancy                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [SKV] token redundancy score, after R-KV: per KV head, a redundancy value
+ * for every cached token computed from the key states alone, with the
+ * attention mask keeping padding out; the final eviction score trades the
+ * token importance against it with sigma (0.1) and tokens are evicted in
+ * ascending order of that score.  Both formulas are printed as images the
+ * text does not reproduce, so the plainest reading of the text is taken:
+ *  [R] cos(a, b) = a.b / (|a| |b|), and 0 when either key is the zero vector;
+ *  [R] r_i = mean over the other valid slots j != i of cos(k_i, k_j): the
+ *      pairwise definition, O(n^2 d) per unit, written out as is;
+ *  [R] r_i = 0 when fewer than two slots are valid (no other key).
+ */
+static double key_norm(const double* x, int d) {
+  double ss = 0.0;
+  for (int e = 0; e < d; ++e) ss += x[e] * x[e];
+  return sqrt(ss);
+}
+
+void kvc_ref_mean_cosine_rows(const uint16_t* k, int T, int d, int pad, const int32_t* rows,
+                              int n_rows, double* r_out) {
+  const int n = T - pad;
+  double* ki = (double*)malloc(sizeof(double) * (size_t)d);
+  double* kj = (double*)malloc(sizeof(double) * (size_t)d);
+  for (int q = 0; q < n_rows; ++q) {
+    const int i = rows[q];
+    if (n < 2) {
+      r_out[q] = 0.0;
+      continue;
+    }
+    for (int e = 0; e < d; ++e) ki[e] = bf16_to_double(k[(size_t)i * d + e]);
+    const double ni = key_norm(ki, d);
+    double sum = 0.0;
+    for (int j = pad; j < T; ++j) {
+      if (j == i) continue;
+      for (int e = 0; e < d; ++e) kj[e] = bf16_to_double(k[(size_t)j * d + e]);
+      const double nj = key_norm(kj, d);
+      if (ni == 0.0 || nj == 0.0) continue; /* cosine 0 */
+      double dot = 0.0;
+      for (int e = 0; e < d; ++e) dot += ki[e] * kj[e];
+      sum += dot / (ni * nj);
+    }
+    r_out[q] = sum / (double)(n - 1);
+  }
+  free(ki);
+  free(kj);
+}
+
+/*
+ * [SKV] final eviction score without the sentence term (sentence similarity
+ * needs text segmentation and hidden states, outside this path):
+ *  [R] R = softmax of r over the valid slots (the redundancy is normalised
+ *      like the importance, so the two are on one scale);
+ *  [R] I_i = s_i / sum over valid v of s_v, s = the max-pooled attention
+ *      usage: the importance normalised over the observation window; I = 0
+ *      when that sum is 0;
+ *  [R] f_i = sigma * I_i - (1 - sigma) * R_i: the more redundant a token,
+ *      the earlier it is evicted.
+ * f replaces the score in the segment-local selection only; segments and
+ * quotas stay on the attention mass ([AMS] Method: the mass and the score
+ * are separate inputs, and any base scorer can supply the score).
+ */
+void kvc_ref_redundancy_score(const uint16_t* k, const float* score, int T, int d, int pad,
+                              double sigma, double* r_out, double* R_out, double* f_out) {
+  const int n = T - pad;
+  double* r = (double*)calloc((size_t)(T > 0 ? T : 1), sizeof(double));
+  int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  for (int i = 0; i < n; ++i) rows[i] = pad + i;
+  if (n > 0) kvc_ref_mean_cosine_rows(k, T, d, pad, rows, n, r + pad);
+  double z = 0.0, s_sum = 0.0;
+  for (int i = pad; i < T; ++i) {
+    z += exp(r[i]);
+    s_sum += (double)score[i];
+  }
+  for (int i = 0; i < T; ++i) {
+    if (i < pad) {
+      if (r_out) r_out[i] = 0.0;
+      if (R_out) R_out[i] = 0.0;
+      if (f_out) f_out[i] = -INFINITY;
+      continue;
+    }
+    const double Ri = exp(r[i]) / z;
+    const double Ii = s_sum > 0.0 ? (double)score[i] / s_sum : 0.0;
+    if (r_out) r_out[i] = r[i];
+    if (R_out) R_out[i] = Ri;
+    if (f_out) f_out[i] = sigma * Ii - (1.0 - sigma) * Ri;
+  }
+  free(r);
+  free(rows);
+}
+
+/* ------------------------------------------------------------------------ */
 /* batched mirrors                                                            */
 /* ------------------------------------------------------------------------ */
 

@@ -57,6 +57,7 @@ typedef struct {
   int seg_fixed;    /* ablation: > 0 = fixed-length segments               */
   int quota_by_len; /* ablation: 1 = quotas by segment length, not mass    */
   int global_topk;  /* ablation: 1 = one segment over all valid slots      */
+  float redundancy_sigma; /* > 0: select on the redundancy-mixed score    */
 } kvc_ref_config;
 
 /* ---- per-unit steps, fp64 (for the pins) -------------------------------- */
@@ -151,6 +152,20 @@ int kvc_ref_compact(const kvc_ref_config* cfg, int U, int T, const uint16_t* k,
                     const uint16_t* v, const float* credit_post,
                     const int32_t* kept_idx, const int32_t* n_kept,
                     uint16_t* k_out, uint16_t* v_out, float* credit_out);
+
+/* [SKV] token redundancy (after R-KV): for each row i in rows[0..n_rows),
+ * r_i = mean over the other valid slots j != i of cos(k_i, k_j); k [T][d]
+ * bf16 bits, valid slots [pad, T); a zero key has cosine 0 with every key;
+ * r_i = 0 when fewer than two slots are valid. */
+void kvc_ref_mean_cosine_rows(const uint16_t* k, int T, int d, int pad, const int32_t* rows,
+                              int n_rows, double* r_out);
+
+/* [SKV] redundancy-mixed eviction score of one unit: score [T] (the max-pooled
+ * usage, >= 0 on valid slots).  r_out[T] = r (above), R_out[T] = softmax of r
+ * over the valid slots, f_out[T] = sigma * s_i / sum_v s_v - (1 - sigma) * R_i;
+ * padding slots get r = R = 0 and f = -inf.  Any output may be NULL. */
+void kvc_ref_redundancy_score(const uint16_t* k, const float* score, int T, int d, int pad,
+                              double sigma, double* r_out, double* R_out, double* f_out);
 
 /* [AMS] Appendix E, paged layout: per-head compaction into newly allocated
  * blocks.  Pools k_pool, v_pool: [L][n_blocks][H][bs][d] bf16 bits (in/out);
