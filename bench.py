@@ -48,6 +48,7 @@ KERNEL_SOURCES = {
     "segment_quota": "segment_quota.cu",
     "select_topk": "select.cu",
     "gather_compact": "compact.cu",
+    "redundancy_score": "redundancy.cu",
 }
 
 
@@ -68,7 +69,18 @@ def parse_args():
                     help="compact into a paged KV pool (block size 16) instead of dense caches")
     ap.add_argument("--ablation", choices=sorted(ABLATIONS), default="none",
                     help="time one of the method's ablations (the pages' ablation table)")
+    ap.add_argument("--redundancy", type=float, default=0.0, metavar="SIGMA",
+                    help="select on the SkipKV key-redundancy mix with this sigma (0.1 in the "
+                         "pages); 0 = the attention score alone")
     return ap.parse_args()
+
+
+def method_kw(args):
+    """Config switches shared by both arms: an ablation and the second base score."""
+    kw = dict(ABLATIONS[args.ablation])
+    if args.redundancy > 0:
+        kw["redundancy_sigma"] = args.redundancy
+    return kw
 
 
 # --------------------------------------------------------------------- helpers
@@ -104,6 +116,8 @@ def unit_work(w, T_valid, T):
         "gather_compact": ("hbm", 0.0, 8.0 * Kb * d + 12.0 * Kb),
         # the same rows and credit moved into pool blocks; plus indices validated
         "compact_paged": ("hbm", 0.0, 8.0 * Kb * d + 16.0 * Kb),
+        # K read once; the score read and the mixed score written
+        "redundancy_score": ("hbm", 0.0, 2.0 * T_valid * d + 8.0 * T_valid),
     }
     return flops, ev_bytes, per_kernel
 
@@ -235,7 +249,7 @@ def run_reference(args, w):
     sample_w = wl.scaled(w, n_layers=1, batch=1)
     first = wl.generate(sample_w, device="cpu")
     p = oracle.RefParams(group=w.group, head_dim=w.head_dim, window=w.window, budget=w.budget,
-                         n_sink=w.n_sink, n_recent=w.n_recent, **ABLATIONS[args.ablation])
+                         n_sink=w.n_sink, n_recent=w.n_recent, **method_kw(args))
 
     def unit_inputs(inp):
         return (wl.bf16_bits(wl.q_units(inp.q, inp.w)), wl.bf16_bits(wl.units_of(inp.k, inp.w)),
@@ -280,7 +294,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": workload_config(w, T, args.ablation),
+        "config": workload_config(w, T, args.ablation, redundancy=args.redundancy),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -288,7 +302,7 @@ def run_reference(args, w):
     print(json.dumps(line))
 
 
-def workload_config(w, T, ablation="none", paged=False):
+def workload_config(w, T, ablation="none", paged=False, redundancy=0.0):
     cfg = {"workload": (f"{w.name}: {w.n_layers} layers x batch {w.batch} x {w.n_kv_heads} KV heads"
                          f" (GQA {w.group}), d {w.head_dim}, {T} slots -> budget {w.budget}, "
                          f"window {w.window}" + (", event 2 (credit carried, 512 fresh slots)"
@@ -298,6 +312,9 @@ def workload_config(w, T, ablation="none", paged=False):
             "l2": "inputs larger than L2 (no flush needed)"}
     if ablation != "none":
         cfg["ablation"] = f"{ablation}: {ABLATIONS[ablation]}"
+    if redundancy > 0:
+        cfg["score"] = (f"SkipKV key-redundancy mix, sigma {redundancy}: "
+                        "sigma * score/sum(score) - (1 - sigma) * softmax(mean key cosine)")
     if paged:
         cfg["paged"] = "compaction into a paged pool, block size 16 (stack and table restored per step)"
     return cfg
@@ -326,7 +343,7 @@ def run_ours(args, w):
     T = first.T
     cfg = kvc.Config(w.n_layers, w.batch, w.n_kv_heads, w.group, w.head_dim,
                      max(T, w.budget + w.interval), w.budget, window=w.window, n_sink=w.n_sink,
-                     n_recent=w.n_recent, **ABLATIONS[args.ablation])
+                     n_recent=w.n_recent, **method_kw(args))
     h = kvc.Handle(cfg)
     inp = first
     if w.n_events > 1:
@@ -512,7 +529,7 @@ def run_ours(args, w):
         oracle.build()
         p = oracle.RefParams(group=w.group, head_dim=w.head_dim, window=w.window,
                              budget=w.budget, n_sink=w.n_sink, n_recent=w.n_recent,
-                             **ABLATIONS[args.ablation])
+                             **method_kw(args))
         q_u = wl.q_units(inp.q, w)
         k_u = wl.units_of(inp.k, w)
         v_u = wl.units_of(inp.v, w)
@@ -542,7 +559,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w, T, args.ablation, args.paged),
+        "config": dict(workload_config(w, T, args.ablation, args.paged, args.redundancy),
                        parallelism=f"replicas x{world}"),
         "roofline": roofline, "event_roofline": event_roofline,
         "kernels": [{k2: (round(v, 6) if isinstance(v, float) else v) for k2, v in r.items()}

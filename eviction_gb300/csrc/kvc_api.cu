@@ -58,6 +58,8 @@ int validate_config(const kvc_config* c, std::string* why) {
   if ((c->quota_by_len != 0 && c->quota_by_len != 1) ||
       (c->global_topk != 0 && c->global_topk != 1))
     return bad("quota_by_len and global_topk must be 0 or 1");
+  if (!(c->redundancy_sigma >= 0.f && c->redundancy_sigma <= 1.f))
+    return bad("redundancy_sigma must lie in [0, 1] (0 = off)");
   if (c->head_dim != 64 && c->head_dim != 128) {
     *why = "head_dim must be 64 or 128";
     return KVC_ERR_UNSUPPORTED;
@@ -89,7 +91,8 @@ int cuda_fail(kvc_handle* h, cudaError_t e, const char* where) {
 
 const char* const kKernelNames[kvc::kNumKernels] = {
     "usage_pass1_rowstats_tcgen05", "usage_pass2_colsum_tcgen05", "mass_pool_ema",
-    "segment_quota", "select_topk", "gather_compact", "refresh_trigger", "compact_paged"};
+    "segment_quota", "select_topk", "gather_compact", "refresh_trigger", "compact_paged",
+    "redundancy_score"};
 
 cudaEvent_t prof_event(kvc_handle* h) {
   auto& P = h->prof;
@@ -176,6 +179,15 @@ int run_select(kvc_handle* h, const float* score, int T, const int32_t* pad,
                                      kept_idx, n_kept, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "select");
   mark_end(h, kvc::kKernelSelect, b, s);
+  return KVC_OK;
+}
+
+int run_redundancy(kvc_handle* h, const uint16_t* k, const float* score, int T,
+                   const int32_t* pad, float* sel, float* red, cudaStream_t s) {
+  cudaEvent_t b = mark_begin(h, s);
+  cudaError_t e = kvc::launch_redundancy(h, k, score, T, pad, sel, red, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "redundancy score");
+  mark_end(h, kvc::kKernelRedundancy, b, s);
   return KVC_OK;
 }
 
@@ -274,7 +286,8 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
   const size_t smem_max = prop.sharedMemPerBlockOptin;
   if (kvc::attention_usage_smem_bytes(d.d, d.R) > smem_max ||
       kvc::segment_smem_bytes(*cfg, cfg->max_T) > smem_max - 16 * 1024 ||
-      kvc::select_smem_bytes(*cfg, cfg->max_T) > smem_max - 1024) {
+      kvc::select_smem_bytes(*cfg, cfg->max_T) > smem_max - 1024 ||
+      kvc::redundancy_smem_bytes(d.d, cfg->max_T) > smem_max) {
     delete h;
     std::fprintf(stderr, "kvc_create: configuration needs more shared memory than the device has\n");
     return KVC_ERR_UNSUPPORTED;
@@ -424,6 +437,24 @@ int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
                      static_cast<cudaStream_t>(stream));
 }
 
+int kvc_redundancy_score(kvc_handle* h, const uint16_t* k, const float* score, int T,
+                         const int32_t* pad, float* sel_score, float* redundancy,
+                         void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  if (!(h->cfg.redundancy_sigma > 0.f))
+    return fail(h, KVC_ERR_ARG, "redundancy_sigma is 0: the redundancy score is off");
+  KVC_REQUIRE_PTR(k);
+  KVC_REQUIRE_PTR(score);
+  KVC_REQUIRE_PTR(pad);
+  KVC_REQUIRE_PTR(sel_score);
+  if (redundancy && !aligned16(redundancy))
+    return fail(h, KVC_ERR_ALIGN, "not 16-byte aligned: redundancy");
+  return run_redundancy(h, k, score, T, pad, sel_score, redundancy,
+                        static_cast<cudaStream_t>(stream));
+}
+
 int kvc_compact_paged(kvc_handle* h, uint16_t* k_pool, uint16_t* v_pool, int n_blocks,
                       int block_size, int max_blocks, const int32_t* seq_len,
                       const int32_t* pad, const int32_t* kept_idx, const int32_t* n_kept,
@@ -502,6 +533,10 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_
   if (rc) return rc;
   rc = run_segment_quota(h, w.mass, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, s);
   if (rc) return rc;
+  if (h->cfg.redundancy_sigma > 0.f) {  // the selection score, in place
+    rc = run_redundancy(h, k, w.score, T, pad, w.score, nullptr, s);
+    if (rc) return rc;
+  }
   rc = run_select(h, w.score, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, kept_idx,
                   n_kept, s);
   if (rc) return rc;

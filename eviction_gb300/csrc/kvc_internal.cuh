@@ -51,6 +51,7 @@ enum KernelId {
   kKernelCompact,
   kKernelRefresh,
   kKernelCompactPaged,
+  kKernelRedundancy,
   kNumKernels
 };
 
@@ -141,6 +142,12 @@ cudaError_t launch_compact_paged(const kvc_handle* h, const PagedArgs& a, cudaSt
 
 cudaError_t launch_refresh(const kvc_handle* h, const uint16_t* q, float* q_ref,
                            float threshold, int32_t* flag, float* sim, cudaStream_t s);
+
+// SkipKV key-redundancy score mixed into the selection score (sel may alias
+// score); red (optional) receives the softmax-normalised redundancy.
+cudaError_t launch_redundancy(const kvc_handle* h, const uint16_t* k, const float* score, int T,
+                              const int32_t* pad, float* sel, float* red, cudaStream_t s);
+size_t redundancy_smem_bytes(int D, int T);
 
 inline int s_max_of(const kvc_config& c, int T) {
   int s = T / c.seg_min;

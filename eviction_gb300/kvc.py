@@ -20,7 +20,7 @@ ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_si
                 "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
                 "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
                 "kvc_profile_read", "kvc_mass_noalloc", "kvc_refresh_decision",
-                "kvc_compact_paged")
+                "kvc_compact_paged", "kvc_redundancy_score")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -141,6 +141,7 @@ def load_library():
     L.kvc_refresh_decision.argtypes = [_P, _P, _P, ctypes.c_float, _P, _P, _P]
     L.kvc_compact_paged.argtypes = [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                                     _P, _P, _P]
+    L.kvc_redundancy_score.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P]
     L.kvc_status_string.argtypes = [_I]
     L.kvc_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -275,6 +276,19 @@ class Handle:
             _dev(kept_idx, torch.int32, "kept_idx"), _dev(n_kept, torch.int32, "n_kept"),
             _stream_ptr(stream))
         self._check(rc, "kvc_event")
+
+    def redundancy_score(self, k, score, T, pad, sel_score, redundancy=None, stream=None):
+        """kvc_redundancy_score: k [L,B,H,T,d] bf16, score [L,B,H,T] fp32 ->
+        sel_score [L,B,H,T] fp32 (may be score itself), redundancy (optional)
+        [L,B,H,T] fp32.  Needs cfg.redundancy_sigma > 0."""
+        import torch
+        red = _dev(redundancy, torch.float32, "redundancy") if redundancy is not None \
+            else ctypes.c_void_p(0)
+        rc = load_library().kvc_redundancy_score(
+            self._h, _dev(k, torch.bfloat16, "k"), _dev(score, torch.float32, "score"), T,
+            _dev(pad, torch.int32, "pad"), _dev(sel_score, torch.float32, "sel_score"), red,
+            _stream_ptr(stream))
+        self._check(rc, "kvc_redundancy_score")
 
     def refresh_decision(self, q, q_ref, threshold, flag, sim, stream=None):
         """kvc_refresh_decision: q [L,B,H*G,d] bf16 (the current token), q_ref

@@ -170,7 +170,29 @@ int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
                 const int32_t* n_kept, uint16_t* k_out, uint16_t* v_out,
                 float* credit_out, void* stream);
 
-/* The whole event, steps 1-6, with the intermediates in the workspace. */
+/* Second base score ("SkipKV: ...", A2 token redundancy score after R-KV, and
+ * the final eviction score without its sentence term), for every unit:
+ *   r_i = mean over the other valid slots j != i of cos(k_i, k_j)
+ *         (a zero key has cosine 0 with every key; r = 0 below two valid slots),
+ *   R_i = exp(r_i) / sum over valid v of exp(r_v),
+ *   I_i = score_i / sum over valid v of score_v   (0 when that sum is 0),
+ *   sel_score_i = sigma * I_i - (1 - sigma) * R_i,  sigma = cfg.redundancy_sigma;
+ * padding slots get sel_score = -inf and redundancy = 0.  Computed in O(T d)
+ * per unit through sum_j cos(k_i, k_j) = (k_i/|k_i|) . (sum_j k_j/|k_j|) - 1,
+ * fp32 arithmetic.
+ *   k          [L][B][H][T][d] bf16, as for kvc_mass;
+ *   score      [L][B][H][T] fp32, >= 0 on valid slots (kvc_mass's score);
+ *   sel_score  [L][B][H][T] fp32 out (may alias score);
+ *   redundancy [L][B][H][T] fp32 out, R; may be NULL.
+ * Needs cfg.redundancy_sigma > 0 (else KVC_ERR_ARG).  kvc_event runs it between
+ * steps 4 and 5 whenever redundancy_sigma > 0; segments and quotas stay on the
+ * attention mass.  Device pointers, caller-owned; asynchronous on `stream`. */
+int kvc_redundancy_score(kvc_handle* h, const uint16_t* k, const float* score, int T,
+                         const int32_t* pad, float* sel_score, float* redundancy,
+                         void* stream);
+
+/* The whole event, steps 1-6, with the intermediates in the workspace.  With
+ * cfg.redundancy_sigma > 0, step 5 selects on kvc_redundancy_score's mix. */
 int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
               const uint16_t* v, int T, const int32_t* pad,
               const int32_t* n_carry, const float* credit_in,
