@@ -10,18 +10,19 @@
 // The mean cosine needs no n x n similarity matrix.  With k^_j = k_j / |k_j|
 // (the zero vector for a zero key) and S = sum over the valid j of k^_j,
 //     sum over j != i of cos(k_i, k_j) = k^_i . S - [k_i != 0]
-// exactly, so a unit costs O(n d) and the kernel is bound by reading K once.
+// exactly, so a unit costs O(n d).
 //
-// Work layout.  One thread-block cluster of C CTAs (C = 1, 2, 4 or 8) per unit;
-// CTA c owns a contiguous slice of the unit's valid rows.  The slice arrives in
-// shared memory by 1-D bulk async copies in 16 KB chunks.  When the slice fits
-// (up to 96 KB; two CTAs per SM), every chunk has its own buffer and stays
-// resident, so K crosses HBM exactly once; a longer slice is streamed twice
-// through a ring of chunk buffers.  The CTAs combine their partial S, and later
-// their partial sums of e^r and of the score, by reading each other's shared
-// memory (DSMEM) in rank order, so every CTA holds bit-identical totals and
-// repeated calls give the same bits.  Every mbarrier wait is bounded; all CTAs
-// of a cluster pass the same cluster barriers whatever happens.
+// Work layout: persistent CTAs, one unit at a time each.  A producer warp
+// streams the unit's valid key rows through a ring of 24 KB shared-memory
+// chunks by 1-D bulk async copies, twice: pass A (row norms, S) and pass B
+// (k^_i . S).  It runs ahead across passes and units, so the ring never
+// drains; the second read of a unit comes a few hundred KB after the first and
+// is served by L2 (the first read is tagged evict-last, the second
+// evict-first).  Twelve consumer warps take a chunk when its copy lands and
+// free it with one arrival per warp.  Per row, 1/|k| and e^r go to device
+// scratch (L2-resident); the sums over the unit (S, sum e^r, sum score) are
+// fixed-order trees, so repeated calls give the same bits.  Every wait is
+// bounded and reports through the status word.
 #include <cmath>
 
 #include "kvc_internal.cuh"
@@ -29,369 +30,372 @@
 namespace kvc {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kChunkBytes = 16384;
-constexpr int kMaxCluster = 8;
-constexpr int kResidentChunks = 6;  // 96 KB: the slice stays in shared memory
-constexpr int kStreamStages = 6;    // ring depth when it does not
+constexpr int kConsumerWarps = 12;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;  // + the producer warp
+constexpr int kChunkBytes = 24576;         // 96 rows of d 128, 192 of d 64: two consumer steps
+constexpr int kStages = 4;
+constexpr int kEpl = 16;                   // key elements per lane and row (two 16-byte loads)
+constexpr int kBarConsumers = 1;           // named barrier of the consumer warps
 
 struct RedArgs {
   const uint16_t* k;
   const float* score;
   const int32_t* pad;
-  float* sel;    // may alias score
-  float* red;    // optional R output
-  int T, B, H, C;
-  int slice_cap;  // rows of the longest slice any unit can have
-  int n_stages;
-  int resident;
+  float* sel;     // may alias score
+  float* red;     // optional R output
+  float* rinv;    // [U][T] scratch: 1/|k| per slot
+  float* rexp;    // [U][T] scratch: e^r per slot
+  int T, B, H, U;
   float sigma;
   uint32_t* status;
 };
 
-// Shared-memory carve-up, identical on host and device.
-struct RedLayout {
-  size_t stages, sacc, spart, stot, ebuf, sbuf, xs, bars, abort_flag, bytes;
-  __host__ __device__ RedLayout(int D, int n_stages, int slice_cap) {
-    size_t o = 0;
-    stages = o;
-    o += static_cast<size_t>(n_stages) * kChunkBytes;
-    sacc = o;                                        // [kWarps][D] per-warp partial S
-    o += static_cast<size_t>(kWarps) * D * 4;
-    spart = o;                                       // [D] this CTA's partial S
-    o += static_cast<size_t>(D) * 4;
-    stot = o;                                        // [D] S of the unit
-    o += static_cast<size_t>(D) * 4;
-    ebuf = o;                                        // [slice_cap] e^{r}
-    o += (static_cast<size_t>(slice_cap) * 4 + 15) & ~size_t(15);
-    sbuf = o;                                        // [slice_cap] score
-    o += (static_cast<size_t>(slice_cap) * 4 + 15) & ~size_t(15);
-    xs = o;                                          // [2] partial sums; [2*kWarps] warp sums
-    o += (2 + 2 * kWarps) * 4;
-    o = (o + 7) & ~size_t(7);
-    bars = o;
-    o += static_cast<size_t>(n_stages) * 8;
-    abort_flag = o;
-    o += 16;
-    bytes = o;
-  }
+template <int D>
+struct Geo {
+  static constexpr int kLpr = D / kEpl;                    // lanes per row: 8 (d 128), 4 (d 64)
+  static constexpr int kRpw = 32 / kLpr;                   // rows per warp and step
+  static constexpr int kRowsStep = kConsumerWarps * kRpw;  // rows per consumer step
+  static constexpr int kChunkRows = kChunkBytes / (D * 2);
+  static constexpr int kSteps = kChunkRows / kRowsStep;    // 2
+  static constexpr int kGroups = kRpw / 4;                 // row groups per warp after two folds
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+struct RedSmem {
+  static constexpr size_t ring = 0;
+  static constexpr size_t sacc = ring + static_cast<size_t>(kStages) * kChunkBytes;  // [12][128]
+  static constexpr size_t stot = sacc + kConsumerWarps * 128 * 4;                     // [128]
+  static constexpr size_t wsum = stot + 128 * 4;                                      // [12][2]
+  static constexpr size_t full = wsum + kConsumerWarps * 2 * 4;
+  static constexpr size_t empty = full + kStages * 8;
+  static constexpr size_t abort_flag = empty + kStages * 8;
+  static constexpr size_t bytes = abort_flag + 16;
+};
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
-// Every thread of every CTA of the cluster arrives, then waits (release /
-// acquire: shared-memory writes before the barrier are visible to the peers'
-// DSMEM reads after it).
-__device__ __forceinline__ void cluster_sync_all() {
-  __syncwarp();  // the .aligned forms need a converged warp
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// fp32 at the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ float ld_peer(const float* p, uint32_t rank) {
-  uint32_t addr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-// 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
+// 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16),
+// with an L2 cache policy.
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
+                                          uint64_t* bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
-__device__ __forceinline__ void unpack8(const uint4 raw, float (&x)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kBarConsumers), "n"(kConsumers) : "memory");
+}
+
+// The valid rows [pad, T) of unit u.
+__device__ __forceinline__ int unit_pad(const RedArgs& a, int u) {
+  return min(max(a.pad[(u / a.H) % a.B], 0), a.T);
+}
+
+// 16 bf16 of one row held by one lane as 8 fp32 pairs: elements [8 sub, 8 sub + 8)
+// and [D/2 + 8 sub, D/2 + 8 sub + 8).
+__device__ __forceinline__ void unpack16(const uint4 w0, const uint4 w1, float2 (&x)[8]) {
+  const uint32_t w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  for (int j = 0; j < 8; ++j)
+    x[j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint4 lds4(const uint16_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// Pass A, one row: acc += k / |k|; returns 1/|k| (0 for a zero key).
+template <int D>
+__device__ __forceinline__ float pass_a_row(const uint4 w0, const uint4 w1, float2 (&acc)[8]) {
+  float2 x[8];
+  unpack16(w0, w1, x);
+  float2 sa = make_float2(0.f, 0.f), sb = sa;  // two chains: half the latency
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    sa = fma2(x[j], x[j], sa);
+    sb = fma2(x[j + 1], x[j + 1], sb);
+  }
+  const float2 s2 = add2(sa, sb);
+  float ss = s2.x + s2.y;
+#pragma unroll
+  for (int o = Geo<D>::kLpr / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+  const float2 iv = make_float2(inv, inv);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = fma2(x[j], iv, acc[j]);
+  return inv;
+}
+
+// Pass B, one row: k . S.
+template <int D>
+__device__ __forceinline__ float pass_b_row(const uint4 w0, const uint4 w1, const float2 (&sv)[8]) {
+  float2 x[8];
+  unpack16(w0, w1, x);
+  float2 da = make_float2(0.f, 0.f), db = da;
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    da = fma2(x[j], sv[j], da);
+    db = fma2(x[j + 1], sv[j + 1], db);
+  }
+  const float2 d2 = add2(da, db);
+  float dot = d2.x + d2.y;
+#pragma unroll
+  for (int o = Geo<D>::kLpr / 2; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  return dot;
+}
+
+// Rows of one chunk for this lane: calls f(row_in_chunk, w0, w1, ok) per
+// consumer step; a full chunk is unrolled without row guards.
+template <int D, typename F>
+__device__ __forceinline__ void for_chunk_rows(const uint16_t* buf, int rows, int grp, int sub,
+                                               F&& f) {
+  using G = Geo<D>;
+  if (rows == G::kChunkRows) {
+    uint4 w[G::kSteps][2];
+#pragma unroll
+    for (int st = 0; st < G::kSteps; ++st) {
+      const uint16_t* row = buf + (st * G::kRowsStep + grp) * D;
+      w[st][0] = lds4(row + sub * 8);
+      w[st][1] = lds4(row + D / 2 + sub * 8);
+    }
+#pragma unroll
+    for (int st = 0; st < G::kSteps; ++st) f(st * G::kRowsStep + grp, w[st][0], w[st][1], true);
+    return;
+  }
+  for (int base = 0; base < rows; base += G::kRowsStep) {
+    const int r = base + grp;
+    const bool ok = r < rows;
+    uint4 w0 = make_uint4(0u, 0u, 0u, 0u), w1 = w0;
+    if (ok) {
+      w0 = lds4(buf + r * D + sub * 8);
+      w1 = lds4(buf + r * D + D / 2 + sub * 8);
+    }
+    f(r, w0, w1, ok);
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) redundancy_kernel(const RedArgs a) {
-  constexpr int kLpr = D / 8;                  // lanes per key row (8 bf16 each)
-  constexpr int kRpw = 32 / kLpr;              // rows per warp and step
-  constexpr int kRowsStep = kWarps * kRpw;     // rows per CTA step
-  constexpr int kChunkRows = kChunkBytes / (D * 2);
-
+  using G = Geo<D>;
   extern __shared__ __align__(128) unsigned char smem[];
-  const RedLayout lay(D, a.n_stages, a.slice_cap);
-  unsigned char* stage_base = smem + lay.stages;
-  float* sacc = reinterpret_cast<float*>(smem + lay.sacc);
-  float* spart = reinterpret_cast<float*>(smem + lay.spart);
-  float* stot = reinterpret_cast<float*>(smem + lay.stot);
-  float* ebuf = reinterpret_cast<float*>(smem + lay.ebuf);
-  float* sbuf = reinterpret_cast<float*>(smem + lay.sbuf);
-  float* xs = reinterpret_cast<float*>(smem + lay.xs);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + lay.abort_flag);
+  unsigned char* ring = smem + RedSmem::ring;
+  float* sacc = reinterpret_cast<float*>(smem + RedSmem::sacc);
+  float* stot = reinterpret_cast<float*>(smem + RedSmem::stot);
+  float* wsum = reinterpret_cast<float*>(smem + RedSmem::wsum);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + RedSmem::full);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + RedSmem::empty);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + RedSmem::abort_flag);
 
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int grp = warp * kRpw + lane / kLpr;   // row group within a step
-  const int sub = lane % kLpr;                 // dims [8 sub, 8 sub + 8)
-  const int C = a.C, T = a.T;
-  const int u = blockIdx.x / C;
-  const uint32_t rank = cluster_rank();
-  const int b = (u / a.H) % a.B;
-  const int pad = min(max(a.pad[b], 0), T);
-  const int n = T - pad;
-  const int slice = (n + C - 1) / C;
-  const int r0 = min(n, static_cast<int>(rank) * slice);
-  const int my = min(n, r0 + slice) - r0;
-  const int nch = (my + kChunkRows - 1) / kChunkRows;
-  const int NS = a.n_stages;
-  const int total_seq = a.resident ? nch : 2 * nch;
-  const uint16_t* krow0 = a.k + (static_cast<size_t>(u) * T + pad + r0) * D;
-
-  auto chunk_rows = [&](int c) { return min(kChunkRows, my - c * kChunkRows); };
-  auto stage_ptr = [&](int s) {
-    return reinterpret_cast<const uint16_t*>(stage_base + static_cast<size_t>(s) * kChunkBytes);
-  };
-  // Issue the copy of sequence item g (chunk g, or chunk g - nch on the second
-  // streamed pass) into its ring slot; thread 0 only, in order g = 0, 1, ...
-  int n_issued = 0;
-  auto issue = [&](int g) {
-    n_issued = g + 1;
-    const int c = g < nch ? g : g - nch;
-    const int s = g % NS;
-    const uint32_t bytes = static_cast<uint32_t>(chunk_rows(c)) * D * 2;
-    mbar_arrive_expect_tx(&bars[s], bytes);
-    bulk_copy(stage_base + static_cast<size_t>(s) * kChunkBytes,
-              krow0 + static_cast<size_t>(c) * kChunkRows * D, bytes, &bars[s]);
-  };
-
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
-    // A wait that already timed out in this launch (or an unread earlier
-    // failure) stops the CTA before it issues any copy: the result is invalid
-    // anyway, and the error stays in the status word.
-    *abort_flag = (*reinterpret_cast<volatile uint32_t*>(a.status) & KVC_STATUS_WAIT_TIMEOUT) ? 1 : 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    // A timeout already recorded (by this launch or an unread earlier failure)
+    // stops the CTA before it issues any copy: the result is invalid anyway.
+    *abort_flag =
+        (*reinterpret_cast<const volatile uint32_t*>(a.status) & KVC_STATUS_WAIT_TIMEOUT) ? 1 : 0;
     fence_barrier_init();
   }
   __syncthreads();
-  if (tid == 0 && !*abort_flag)
-    for (int g = 0; g < min(NS, total_seq); ++g) issue(g);
 
-  // ---- pass A: S = sum of the unit-normalised keys ---------------------------
-  float acc[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const int g = c, s = g % NS;
-    mbar_wait(&bars[s], (g / NS) & 1, abort_flag, a.status);
-    const uint16_t* buf = stage_ptr(s);
-    const int rows = chunk_rows(c);
-    for (int base = 0; base < rows; base += kRowsStep) {
-      const int r = base + grp;
-      const uint4 raw = r < rows ? *reinterpret_cast<const uint4*>(buf + r * D + sub * 8)
-                                 : make_uint4(0u, 0u, 0u, 0u);
-      float x[8];
-      unpack8(raw, x);
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-      for (int o = kLpr / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float inv = ss > 0.f ? 1.0f / sqrtf(ss) : 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fmaf(x[e], inv, acc[e]);
-    }
-    if (!a.resident) {
-      __syncthreads();  // every thread is done with slot s
-      if (tid == 0 && g + NS < total_seq && !*abort_flag) issue(g + NS);
-    }
-  }
-  // Combine the row groups of a warp (lanes with the same dims), then warps.
-#pragma unroll
-  for (int o = kLpr; o < 32; o <<= 1)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
-  if (lane < kLpr) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) sacc[warp * D + sub * 8 + e] = acc[e];
-  }
-  __syncthreads();
-  for (int t = tid; t < D; t += kThreads) {
-    float v = 0.f;
-    for (int w = 0; w < kWarps; ++w) v += sacc[w * D + t];
-    spart[t] = v;
-  }
-  cluster_sync_all();
-  for (int t = tid; t < D; t += kThreads) {
-    float v = 0.f;
-    for (int c = 0; c < C; ++c) v += ld_peer(spart + t, static_cast<uint32_t>(c));
-    stot[t] = v;
-  }
-  __syncthreads();
-
-  // ---- pass B: e^{r_i}, r_i = (k^_i . S - 1) / (n - 1) ---------------------------
-  float sv[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) sv[e] = stot[sub * 8 + e];
-  const float inv_nm1 = n >= 2 ? 1.0f / static_cast<float>(n - 1) : 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const int g = a.resident ? c : nch + c, s = g % NS;
-    if (!a.resident) mbar_wait(&bars[s], (g / NS) & 1, abort_flag, a.status);
-    const uint16_t* buf = stage_ptr(s);
-    const int rows = chunk_rows(c);
-    for (int base = 0; base < rows; base += kRowsStep) {
-      const int r = base + grp;
-      const uint4 raw = r < rows ? *reinterpret_cast<const uint4*>(buf + r * D + sub * 8)
-                                 : make_uint4(0u, 0u, 0u, 0u);
-      float x[8];
-      unpack8(raw, x);
-      float ss = 0.f, dot = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ss = fmaf(x[e], x[e], ss);
-        dot = fmaf(x[e], sv[e], dot);
+  if (warp == kConsumerWarps) {
+    // ---- producer: for every unit of this CTA, its chunks twice -------------
+    if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+      int seq = 0;  // ring items issued
+      for (int u = blockIdx.x; u < a.U && !*abort_flag; u += gridDim.x) {
+        const int pad = unit_pad(a, u);
+        const int n = a.T - pad;
+        const int nch = (n + G::kChunkRows - 1) / G::kChunkRows;
+        const uint16_t* src = a.k + (static_cast<size_t>(u) * a.T + pad) * D;
+        for (int g = 0; g < 2 * nch && !*abort_flag; ++g, ++seq) {
+          const int c = g < nch ? g : g - nch;
+          const int s = seq % kStages;
+          if (seq >= kStages &&
+              !mbar_wait(&empty[s], static_cast<uint32_t>(seq / kStages - 1) & 1u, abort_flag,
+                         a.status))
+            break;
+          const uint32_t bytes =
+              static_cast<uint32_t>(min(G::kChunkRows, n - c * G::kChunkRows)) * D * 2;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          bulk_copy(ring + static_cast<size_t>(s) * kChunkBytes,
+                    src + static_cast<size_t>(c) * G::kChunkRows * D, bytes, &full[s],
+                    g < nch ? keep : drop);
+        }
       }
-#pragma unroll
-      for (int o = kLpr / 2; o > 0; o >>= 1) {
-        ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      }
-      if (r < rows && sub == 0) {
-        const float rr = ss > 0.f ? (dot / sqrtf(ss) - 1.0f) * inv_nm1 : 0.f;
-        ebuf[c * kChunkRows + r] = expf(rr);
+      // After an abort, let the copies in flight land before the shared memory
+      // is released: only the last item of each slot can be outstanding.
+      if (*abort_flag) {
+        const uint64_t t0 = global_timer_ns();
+        for (int s = 0; s < kStages && s < seq; ++s) {
+          const int last = s + kStages * ((seq - 1 - s) / kStages);
+          while (!mbar_test_sleep(&full[s], static_cast<uint32_t>(last / kStages) & 1u,
+                                  kWaitSleepNs) &&
+                 global_timer_ns() - t0 < kWaitLimitNs) {
+          }
+        }
       }
     }
-    if (!a.resident) {
-      __syncthreads();
-      if (tid == 0 && g + NS < total_seq && !*abort_flag) issue(g + NS);
-    }
+    return;
   }
-  __syncthreads();
 
-  // ---- sums of e^r and of the score over the unit, then f ------------------------
-  const float* srow = a.score + static_cast<size_t>(u) * T + pad + r0;
-  float pe = 0.f, ps = 0.f;
-  for (int i = tid; i < my; i += kThreads) {
-    const float sc = srow[i];
-    sbuf[i] = sc;
-    ps += sc;
-    pe += ebuf[i];
-  }
+  // ---- consumers --------------------------------------------------------------
+  const int grp = warp * G::kRpw + lane / G::kLpr;  // row group within a step
+  const int sub = lane % G::kLpr;                   // dims [8 sub, +8) and [D/2 + 8 sub, +8)
+  int seq = 0;                                      // ring items consumed
+  // Wait for ring item `seq`, hand its buffer to f, free the slot.
+  auto take = [&](auto&& f) {
+    const int s = seq % kStages;
+    mbar_wait(&full[s], static_cast<uint32_t>(seq / kStages) & 1u, abort_flag, a.status);
+    f(reinterpret_cast<const uint16_t*>(ring + static_cast<size_t>(s) * kChunkBytes));
+    __syncwarp();
+    if (lane == 0 && !*abort_flag) mbar_arrive(&empty[s]);
+    ++seq;
+  };
+
+  for (int u = blockIdx.x; u < a.U; u += gridDim.x) {
+    const int pad = unit_pad(a, u);
+    const int n = a.T - pad;
+    const int nch = (n + G::kChunkRows - 1) / G::kChunkRows;
+    const size_t base = static_cast<size_t>(u) * a.T;
+    float* rinv = a.rinv + base + pad;
+    float* rexp = a.rexp + base + pad;
+
+    // pass A: row norms and the per-lane sums of k^
+    float2 acc[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    pe += __shfl_xor_sync(0xffffffffu, pe, o);
-    ps += __shfl_xor_sync(0xffffffffu, ps, o);
-  }
-  float* wsum = xs + 2;
-  if (lane == 0) {
-    wsum[2 * warp] = pe;
-    wsum[2 * warp + 1] = ps;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float e = 0.f, sc = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      e += wsum[2 * w];
-      sc += wsum[2 * w + 1];
+    for (int j = 0; j < 8; ++j) acc[j] = make_float2(0.f, 0.f);
+    for (int c = 0; c < nch; ++c) {
+      const int rows = min(G::kChunkRows, n - c * G::kChunkRows);
+      take([&](const uint16_t* buf) {
+        for_chunk_rows<D>(buf, rows, grp, sub, [&](int r, uint4 w0, uint4 w1, bool ok) {
+          const float inv = pass_a_row<D>(w0, w1, acc);
+          if (ok && sub == 0) rinv[c * G::kChunkRows + r] = inv;
+        });
+      });
     }
-    xs[0] = e;
-    xs[1] = sc;
-  }
-  cluster_sync_all();
-  float z = 0.f, s_tot = 0.f;
-  for (int c = 0; c < C; ++c) {
-    z += ld_peer(xs, static_cast<uint32_t>(c));
-    s_tot += ld_peer(xs + 1, static_cast<uint32_t>(c));
-  }
-  const float inv_z = z > 0.f ? 1.0f / z : 0.f;
-  const float inv_s = s_tot > 0.f ? 1.0f / s_tot : 0.f;
-  const float w_i = a.sigma * inv_s;
-  const float w_r = (1.0f - a.sigma) * inv_z;
-  float* sel = a.sel + static_cast<size_t>(u) * T;
-  float* red = a.red ? a.red + static_cast<size_t>(u) * T : nullptr;
-  for (int i = tid; i < my; i += kThreads) {
-    const float e = ebuf[i];
-    sel[pad + r0 + i] = fmaf(w_i, sbuf[i], -(w_r * e));
-    if (red) red[pad + r0 + i] = e * inv_z;
-  }
-  if (rank == 0) {
-    for (int i = tid; i < pad; i += kThreads) {
+    // S: fold the row groups of each warp twice, then the warps in order
+#pragma unroll
+    for (int o = 16; o >= 8; o >>= 1)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[j].x += __shfl_xor_sync(0xffffffffu, acc[j].x, o);
+        acc[j].y += __shfl_xor_sync(0xffffffffu, acc[j].y, o);
+      }
+    if (lane < 8) {
+      float* dst = sacc + (warp * G::kGroups + lane / G::kLpr) * D;
+      *reinterpret_cast<float4*>(dst + sub * 8) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+      *reinterpret_cast<float4*>(dst + sub * 8 + 4) = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+      *reinterpret_cast<float4*>(dst + D / 2 + sub * 8) =
+          make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
+      *reinterpret_cast<float4*>(dst + D / 2 + sub * 8 + 4) =
+          make_float4(acc[6].x, acc[6].y, acc[7].x, acc[7].y);
+    }
+    consumer_sync();
+    if (tid < D) {
+      float v = 0.f;
+      for (int g = 0; g < kConsumerWarps * G::kGroups; ++g) v += sacc[g * D + tid];
+      stot[tid] = v;
+    }
+    consumer_sync();
+    float2 sv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = (j < 4 ? sub * 8 : D / 2 + sub * 8) + 2 * (j % 4);
+      sv[j] = make_float2(stot[e], stot[e + 1]);
+    }
+
+    // pass B: e^{r_i}, r_i = (k_i . S / |k_i| - 1) / (n - 1)
+    const float inv_nm1 = n >= 2 ? 1.0f / static_cast<float>(n - 1) : 0.f;
+    float pe = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const int rows = min(G::kChunkRows, n - c * G::kChunkRows);
+      take([&](const uint16_t* buf) {
+        for_chunk_rows<D>(buf, rows, grp, sub, [&](int r, uint4 w0, uint4 w1, bool ok) {
+          const float dot = pass_b_row<D>(w0, w1, sv);
+          if (ok && sub == 0) {
+            const int i = c * G::kChunkRows + r;
+            const float inv = rinv[i];
+            const float e = __expf(inv > 0.f ? fmaf(dot, inv, -1.0f) * inv_nm1 : 0.f);
+            rexp[i] = e;
+            pe += e;
+          }
+        });
+      });
+    }
+
+    // sums of e^r and of the score over the unit (lanes, warps in order)
+    const float* srow = a.score + base + pad;
+    float ps = 0.f;
+    for (int i = tid; i < n; i += kConsumers) ps += srow[i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      pe += __shfl_xor_sync(0xffffffffu, pe, o);
+      ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    }
+    if (lane == 0) {
+      wsum[2 * warp] = pe;
+      wsum[2 * warp + 1] = ps;
+    }
+    consumer_sync();  // also: every rexp store of the unit is visible below
+    float z = 0.f, s_tot = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      z += wsum[2 * w];
+      s_tot += wsum[2 * w + 1];
+    }
+    const float inv_z = z > 0.f ? 1.0f / z : 0.f;
+    const float w_i = a.sigma * (s_tot > 0.f ? 1.0f / s_tot : 0.f);
+    const float w_r = (1.0f - a.sigma) * inv_z;
+    float* sel = a.sel + base;
+    float* red = a.red ? a.red + base : nullptr;
+    for (int i = tid; i < n; i += kConsumers) {
+      const float e = rexp[i];
+      sel[pad + i] = fmaf(w_i, srow[i], -(w_r * e));
+      if (red) red[pad + i] = e * inv_z;
+    }
+    for (int i = tid; i < pad; i += kConsumers) {
       sel[i] = -INFINITY;
       if (red) red[i] = 0.f;
     }
+    consumer_sync();  // sacc, stot and wsum are rewritten by the next unit
   }
-
-  // A wait that gave up may leave copies in flight: let them land (bounded)
-  // before the shared memory is released.  Only the last copy issued into a
-  // slot can be outstanding: a slot is refilled only after all threads saw
-  // its previous copy complete, and nothing is issued after an abort.
-  if (tid == 0 && *abort_flag) {
-    const uint64_t t0 = global_timer_ns();
-    for (int s = 0; s < NS && s < n_issued; ++s) {
-      const int last = s + NS * ((n_issued - 1 - s) / NS);
-      while (!mbar_test_sleep(&bars[s], (last / NS) & 1, kWaitSleepNs) &&
-             global_timer_ns() - t0 < kWaitLimitNs) {
-      }
-    }
-  }
-  cluster_sync_all();  // no peer reads this CTA's shared memory any more
 }
-
-int cdiv(int a, int b) { return (a + b - 1) / b; }
 
 }  // namespace
 
 cudaError_t launch_redundancy(const kvc_handle* h, const uint16_t* k, const float* score, int T,
                               const int32_t* pad, float* sel, float* red, cudaStream_t s) {
   const int D = h->dims.d;
-  const int chunk_rows = kChunkBytes / (D * 2);
-  int C = 1;
-  while (C < kMaxCluster && cdiv(cdiv(T, C), chunk_rows) > kResidentChunks) C *= 2;
-  const int slice_cap = cdiv(T, C);
-  const int nch = cdiv(slice_cap, chunk_rows);
-  const bool resident = nch <= kResidentChunks;
-  RedArgs a{k, score, pad, sel, red, T, h->dims.B, h->dims.H, C, slice_cap,
-            resident ? (nch > 0 ? nch : 1) : kStreamStages, resident ? 1 : 0,
-            h->cfg.redundancy_sigma, h->ws.status};
-  const RedLayout lay(D, a.n_stages, slice_cap);
-  const int smem = static_cast<int>(lay.bytes);
+  // scratch: the workspace's raw-usage and mass arrays, free once the segments
+  // are cut (neither is read after step 4 of the event)
+  RedArgs a{k, score, pad, sel, red, h->ws.usage, h->ws.mass, T, h->dims.B, h->dims.H,
+            h->dims.U, h->cfg.redundancy_sigma, h->ws.status};
+  const int smem = static_cast<int>(RedSmem::bytes);
   void (*kern)(const RedArgs) = D == 64 ? redundancy_kernel<64> : redundancy_kernel<128>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(C) * static_cast<unsigned>(h->dims.U), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, a);
-  return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int fit = per_sm * h->num_sms;
+  const int grid = fit < h->dims.U ? fit : h->dims.U;
+  kern<<<grid, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
 }
 
-size_t redundancy_smem_bytes(int D, int T) {
-  const int chunk_rows = kChunkBytes / (D * 2);
-  int C = 1;
-  while (C < kMaxCluster && cdiv(cdiv(T, C), chunk_rows) > kResidentChunks) C *= 2;
-  const int slice_cap = cdiv(T, C);
-  const int nch = cdiv(slice_cap, chunk_rows);
-  const int ns = nch <= kResidentChunks ? (nch > 0 ? nch : 1) : kStreamStages;
-  return RedLayout(D, ns, slice_cap).bytes;
-}
+size_t redundancy_smem_bytes(int, int) { return RedSmem::bytes; }
 
 }  // namespace kvc

@@ -184,6 +184,7 @@ int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
  *   score      [L][B][H][T] fp32, >= 0 on valid slots (kvc_mass's score);
  *   sel_score  [L][B][H][T] fp32 out (may alias score);
  *   redundancy [L][B][H][T] fp32 out, R; may be NULL.
+ * Uses the handle's workspace as scratch (two fp32 values per slot).
  * Needs cfg.redundancy_sigma > 0 (else KVC_ERR_ARG).  kvc_event runs it between
  * steps 4 and 5 whenever redundancy_sigma > 0; segments and quotas stay on the
  * attention mass.  Device pointers, caller-owned; asynchronous on `stream`. */

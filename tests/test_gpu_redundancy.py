@@ -101,10 +101,13 @@ def _check_unit(f_g, R_g, f_o, R_o, s, pad, sigma):
 
 
 @pytest.mark.parametrize("L,B,H,T,d,pads", [
-    (1, 3, 2, 300, 64, [0, 17, 299]),            # C = 1, ragged, one valid slot
-    (2, 2, 2, 700, 128, [0, 650]),               # C = 2, ragged tail of a chunk
-    (1, 4, 2, 1536, 128, [0, 1, 700, 1536]),     # C = 4 (the 28-layer shape), empty unit
-    (1, 2, 1, 1112, 64, [5, 1000]),              # C = 2 at d 64
+    (1, 3, 2, 300, 64, [0, 17, 299]),            # d 64, ragged, one valid slot
+    (2, 12, 4, 700, 128, [0, 650, 3, 699, 7, 100, 0, 0, 42, 512, 9, 1]),
+                                                 # 96 units: CTAs walk several units each
+                                                 # only when the grid is smaller; ragged tails
+    (1, 2, 2, 2500, 128, [0, 900]),              # many chunks per unit
+    (1, 4, 2, 1536, 128, [0, 1, 700, 1536]),     # the 28-layer shape, an empty unit
+    (1, 2, 1, 1112, 64, [5, 1000]),              # d 64, chunk tails
 ])
 def test_redundancy_matches_oracle(ref, L, B, H, T, d, pads):
     import eviction_gb300 as kvc
@@ -189,6 +192,35 @@ def test_streamed_long_cache_sampled(ref, T, d, pads):
             2 * U32 * np.abs(want)
         assert np.all(np.abs(f[pad:] - want) <= tol)
         assert np.all(np.isneginf(f[:pad]))
+
+
+def test_bench_shape_sampled(ref):
+    """The 28-layer workload's keys (3584 units, T 1536, the launch the event
+    times), a seeded score, 6 sampled units against the oracle."""
+    import eviction_gb300 as kvc
+    w = wl.CONFIGS["qwen_28l"]
+    inp = wl.generate(w, device="cuda")
+    T, U = inp.T, w.units
+    rng = np.random.default_rng(28)
+    score = torch.from_numpy(rng.gamma(0.5, 1.0, (w.n_layers, w.batch, w.n_kv_heads, T))
+                             .astype(np.float32)).cuda()
+    sigma = 0.1
+    h = kvc.Handle(gu.config_for(w, T, redundancy_sigma=sigma))
+    sel = torch.empty_like(score)
+    red = torch.empty_like(score)
+    h.redundancy_score(inp.k, score, T, inp.pad, sel, red)
+    torch.cuda.synchronize()
+    assert h.device_status() == 0
+    units = rng.choice(U, 6, replace=False)
+    idx = torch.as_tensor(units, device="cuda", dtype=torch.long)
+    kb = wl.bf16_bits(wl.units_of(inp.k, w).index_select(0, idx))
+    sc = score.reshape(U, T).index_select(0, idx).cpu().numpy()
+    pad_u = wl.unit_pad(inp).to("cuda").index_select(0, idx).cpu().numpy()
+    f_o, R_o, _ = ref.redundancy_score(kb, sc, pad_u, sigma)
+    f_g = sel.reshape(U, T).index_select(0, idx).cpu().numpy()
+    R_g = red.reshape(U, T).index_select(0, idx).cpu().numpy()
+    for i in range(len(units)):
+        _check_unit(f_g[i], R_g[i], f_o[i], R_o[i], sc[i], int(pad_u[i]), sigma)
 
 
 def test_repeat_runs_identical():
