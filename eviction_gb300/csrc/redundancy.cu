@@ -15,14 +15,16 @@
 // Work layout: persistent CTAs, one unit at a time each.  A producer warp
 // streams the unit's valid key rows through a ring of 24 KB shared-memory
 // chunks by 1-D bulk async copies, twice: pass A (row norms, S) and pass B
-// (k^_i . S).  It runs ahead across passes and units, so the ring never
-// drains; the second read of a unit comes a few hundred KB after the first and
-// is served by L2 (the first read is tagged evict-last, the second
-// evict-first).  Twelve consumer warps take a chunk when its copy lands and
-// free it with one arrival per warp.  Per row, 1/|k| and e^r go to device
-// scratch (L2-resident); the sums over the unit (S, sum e^r, sum score) are
-// fixed-order trees, so repeated calls give the same bits.  Every wait is
-// bounded and reports through the status word.
+// (k^_i . S, chunks newest first).  It runs ahead across passes and units, so
+// the ring never drains; the second read of a unit comes a few hundred KB
+// after the first and is served mostly by L2 (the first read is tagged
+// evict-last, the second evict-first).  Twelve consumer warps take a chunk
+// when its copy lands and free it with one arrival per warp.  Per row, 1/|k|
+// and e^r (and the scores, copied in asynchronously while the passes run)
+// stay in shared memory for units up to 2048 slots, else they use device
+// scratch; the sums over the unit (S, sum e^r, sum score) are fixed-order
+// trees, so repeated calls give the same bits.  Every wait is bounded and
+// reports through the status word.
 #include <cmath>
 
 #include "kvc_internal.cuh"
@@ -34,7 +36,8 @@ constexpr int kConsumerWarps = 12;
 constexpr int kConsumers = 32 * kConsumerWarps;
 constexpr int kThreads = kConsumers + 32;  // + the producer warp
 constexpr int kChunkBytes = 24576;         // 96 rows of d 128, 192 of d 64: two consumer steps
-constexpr int kStages = 4;
+constexpr int kStages = 3;
+constexpr int kRowsCap = 2048;             // units up to this many slots keep per-row values in smem
 constexpr int kEpl = 16;                   // key elements per lane and row (two 16-byte loads)
 constexpr int kBarConsumers = 1;           // named barrier of the consumer warps
 
@@ -59,6 +62,7 @@ struct Geo {
   static constexpr int kChunkRows = kChunkBytes / (D * 2);
   static constexpr int kSteps = kChunkRows / kRowsStep;    // 2
   static constexpr int kGroups = kRpw / 4;                 // row groups per warp after two folds
+  static_assert(kChunkRows % kRowsStep == 0, "a chunk is a whole number of consumer steps");
 };
 
 struct RedSmem {
@@ -69,7 +73,10 @@ struct RedSmem {
   static constexpr size_t full = wsum + kConsumerWarps * 2 * 4;
   static constexpr size_t empty = full + kStages * 8;
   static constexpr size_t abort_flag = empty + kStages * 8;
-  static constexpr size_t bytes = abort_flag + 16;
+  static constexpr size_t rows = abort_flag + 16;  // [3][kRowsCap] 1/|k|, e^r, score (short units)
+  static constexpr size_t bytes(bool rows_in_smem) {
+    return rows + (rows_in_smem ? 3 * kRowsCap * 4 : 0);
+  }
 };
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -92,6 +99,16 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// 4-byte asynchronous global -> shared copies (the unit's scores, landing
+// while the passes run).
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -184,7 +201,9 @@ __device__ __forceinline__ void for_chunk_rows(const uint16_t* buf, int rows, in
   }
 }
 
-template <int D>
+// ROWS: units of up to kRowsCap slots keep 1/|k| and e^r in shared memory,
+// longer ones in the device scratch.
+template <int D, bool ROWS>
 __global__ void __launch_bounds__(kThreads) redundancy_kernel(const RedArgs a) {
   using G = Geo<D>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -221,7 +240,9 @@ __global__ void __launch_bounds__(kThreads) redundancy_kernel(const RedArgs a) {
         const int nch = (n + G::kChunkRows - 1) / G::kChunkRows;
         const uint16_t* src = a.k + (static_cast<size_t>(u) * a.T + pad) * D;
         for (int g = 0; g < 2 * nch && !*abort_flag; ++g, ++seq) {
-          const int c = g < nch ? g : g - nch;
+          // pass B takes the chunks newest first: the most recently read are
+          // the likeliest to still be in L2
+          const int c = g < nch ? g : 2 * nch - 1 - g;
           const int s = seq % kStages;
           if (seq >= kStages &&
               !mbar_wait(&empty[s], static_cast<uint32_t>(seq / kStages - 1) & 1u, abort_flag,
@@ -254,24 +275,36 @@ __global__ void __launch_bounds__(kThreads) redundancy_kernel(const RedArgs a) {
   // ---- consumers --------------------------------------------------------------
   const int grp = warp * G::kRpw + lane / G::kLpr;  // row group within a step
   const int sub = lane % G::kLpr;                   // dims [8 sub, +8) and [D/2 + 8 sub, +8)
-  int seq = 0;                                      // ring items consumed
-  // Wait for ring item `seq`, hand its buffer to f, free the slot.
+  int slot = 0;                                     // ring slot of the next item
+  uint32_t phase = 0;                               // its full-barrier phase parity
+  // Wait for the next ring item, hand its buffer to f, free the slot.  The
+  // first probe suspends until the copy lands (the usual case); the bounded
+  // wait is the fallback.
   auto take = [&](auto&& f) {
-    const int s = seq % kStages;
-    mbar_wait(&full[s], static_cast<uint32_t>(seq / kStages) & 1u, abort_flag, a.status);
-    f(reinterpret_cast<const uint16_t*>(ring + static_cast<size_t>(s) * kChunkBytes));
+    if (!mbar_test_sleep(&full[slot], phase, kWaitSleepNs))
+      mbar_wait(&full[slot], phase, abort_flag, a.status);
+    f(reinterpret_cast<const uint16_t*>(ring + static_cast<size_t>(slot) * kChunkBytes));
     __syncwarp();
-    if (lane == 0 && !*abort_flag) mbar_arrive(&empty[s]);
-    ++seq;
+    if (lane == 0 && !*abort_flag) mbar_arrive(&empty[slot]);
+    if (++slot == kStages) {
+      slot = 0;
+      phase ^= 1u;
+    }
   };
 
+  int pad = blockIdx.x < a.U ? unit_pad(a, blockIdx.x) : 0;
   for (int u = blockIdx.x; u < a.U; u += gridDim.x) {
-    const int pad = unit_pad(a, u);
+    // the next unit's padding, loaded now and used one unit later
+    const int pad_next = u + static_cast<int>(gridDim.x) < a.U ? unit_pad(a, u + gridDim.x) : 0;
     const int n = a.T - pad;
     const int nch = (n + G::kChunkRows - 1) / G::kChunkRows;
     const size_t base = static_cast<size_t>(u) * a.T;
-    float* rinv = a.rinv + base + pad;
-    float* rexp = a.rexp + base + pad;
+    float* rinv = ROWS ? reinterpret_cast<float*>(smem + RedSmem::rows) : a.rinv + base + pad;
+    float* rexp = ROWS ? rinv + kRowsCap : a.rexp + base + pad;
+    const float* srow = a.score + base + pad;
+    float* sscore = rinv + 2 * kRowsCap;  // ROWS only
+    if (ROWS)
+      for (int i = tid; i < n; i += kConsumers) cp_async4(sscore + i, srow + i);
 
     // pass A: row norms and the per-lane sums of k^
     float2 acc[8];
@@ -320,7 +353,8 @@ __global__ void __launch_bounds__(kThreads) redundancy_kernel(const RedArgs a) {
     // pass B: e^{r_i}, r_i = (k_i . S / |k_i| - 1) / (n - 1)
     const float inv_nm1 = n >= 2 ? 1.0f / static_cast<float>(n - 1) : 0.f;
     float pe = 0.f;
-    for (int c = 0; c < nch; ++c) {
+    for (int cc = 0; cc < nch; ++cc) {
+      const int c = nch - 1 - cc;  // the producer's pass-B order
       const int rows = min(G::kChunkRows, n - c * G::kChunkRows);
       take([&](const uint16_t* buf) {
         for_chunk_rows<D>(buf, rows, grp, sub, [&](int r, uint4 w0, uint4 w1, bool ok) {
@@ -337,9 +371,13 @@ __global__ void __launch_bounds__(kThreads) redundancy_kernel(const RedArgs a) {
     }
 
     // sums of e^r and of the score over the unit (lanes, warps in order)
-    const float* srow = a.score + base + pad;
+    const float* sc = srow;
+    if (ROWS) {
+      cp_async_wait_all();  // this thread's score copies (it reads only its own rows)
+      sc = sscore;
+    }
     float ps = 0.f;
-    for (int i = tid; i < n; i += kConsumers) ps += srow[i];
+    for (int i = tid; i < n; i += kConsumers) ps += sc[i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       pe += __shfl_xor_sync(0xffffffffu, pe, o);
@@ -362,14 +400,15 @@ __global__ void __launch_bounds__(kThreads) redundancy_kernel(const RedArgs a) {
     float* red = a.red ? a.red + base : nullptr;
     for (int i = tid; i < n; i += kConsumers) {
       const float e = rexp[i];
-      sel[pad + i] = fmaf(w_i, srow[i], -(w_r * e));
+      sel[pad + i] = fmaf(w_i, sc[i], -(w_r * e));
       if (red) red[pad + i] = e * inv_z;
     }
     for (int i = tid; i < pad; i += kConsumers) {
       sel[i] = -INFINITY;
       if (red) red[i] = 0.f;
     }
-    consumer_sync();  // sacc, stot and wsum are rewritten by the next unit
+    consumer_sync();  // sacc, stot, wsum and the row values are rewritten by the next unit
+    pad = pad_next;
   }
 }
 
@@ -382,8 +421,11 @@ cudaError_t launch_redundancy(const kvc_handle* h, const uint16_t* k, const floa
   // are cut (neither is read after step 4 of the event)
   RedArgs a{k, score, pad, sel, red, h->ws.usage, h->ws.mass, T, h->dims.B, h->dims.H,
             h->dims.U, h->cfg.redundancy_sigma, h->ws.status};
-  const int smem = static_cast<int>(RedSmem::bytes);
-  void (*kern)(const RedArgs) = D == 64 ? redundancy_kernel<64> : redundancy_kernel<128>;
+  const bool rows = T <= kRowsCap;
+  const int smem = static_cast<int>(RedSmem::bytes(rows));
+  void (*kern)(const RedArgs) =
+      D == 64 ? (rows ? redundancy_kernel<64, true> : redundancy_kernel<64, false>)
+              : (rows ? redundancy_kernel<128, true> : redundancy_kernel<128, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
@@ -396,6 +438,6 @@ cudaError_t launch_redundancy(const kvc_handle* h, const uint16_t* k, const floa
   return cudaGetLastError();
 }
 
-size_t redundancy_smem_bytes(int, int) { return RedSmem::bytes; }
+size_t redundancy_smem_bytes(int, int T) { return RedSmem::bytes(T <= kRowsCap); }
 
 }  // namespace kvc
