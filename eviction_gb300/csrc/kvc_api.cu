@@ -492,6 +492,13 @@ int kvc_compact_paged(kvc_handle* h, uint16_t* k_pool, uint16_t* v_pool, int n_b
   return KVC_OK;
 }
 
+int kvc_wait_self_test(kvc_handle* h, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  cudaError_t e = kvc::launch_wait_self_test(h, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e, "wait self-test");
+  return KVC_OK;
+}
+
 int kvc_refresh_decision(kvc_handle* h, const uint16_t* q, float* q_ref, float threshold,
                          int32_t* flag, float* sim, void* stream) {
   if (!h) return KVC_ERR_ARG;

@@ -149,6 +149,9 @@ cudaError_t launch_redundancy(const kvc_handle* h, const uint16_t* k, const floa
                               const int32_t* pad, float* sel, float* red, cudaStream_t s);
 size_t redundancy_smem_bytes(int D, int T);
 
+// One thread waits (bounded) on a barrier nothing completes: the timeout path.
+cudaError_t launch_wait_self_test(const kvc_handle* h, cudaStream_t s);
+
 inline int s_max_of(const kvc_config& c, int T) {
   int s = T / c.seg_min;
   return s > 1 ? s : 1;

@@ -16,7 +16,8 @@
 //      call's error word; nothing below changes anything then);
 //   2. allocate (one CTA): a block scan of ceil(n_kept_b / bs) over sequences
 //      takes the top entries of the stack in sequence order -- deterministic;
-//   3. copy kept rows (16-byte vectors), plus the dense credit gather;
+//   3. copy kept rows (row offsets resolved once into shared memory, then
+//      16-byte vectors with several loads in flight), plus the dense credit gather;
 //   4. free (one CTA): push each sequence's old blocks in sequence order.
 // Old and new blocks coexist between 2 and 4, as the appendix notes.
 #include "kvc_internal.cuh"
@@ -145,35 +146,73 @@ __global__ void __launch_bounds__(kScanThreads) paged_alloc_kernel(PagedParams p
 }
 
 // grid (ceil(budget / rows_per_cta), L*B*H); 16-byte vectors, rows_per_cta rows
-__global__ void paged_copy_kernel(PagedParams p, int rows_per_cta) {
-  if (*p.err) return;
+constexpr int kCopyRows = 64;      // kept rows per CTA
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;     // 16-byte loads in flight per thread
+
+// Copy kept rows into the new blocks.  The row offsets (source position in an
+// old block, destination row of a new block) and the credit are resolved once
+// per row into shared memory; the rows then move as 16-byte vectors with
+// several loads in flight per thread.  Old and new blocks are disjoint (new
+// blocks come off the free stack), so reads and writes never overlap.
+__global__ void __launch_bounds__(kCopyThreads) paged_copy_kernel(PagedParams p, int vpr_log2) {
+  __shared__ long long s_src[kCopyRows], s_dst[kCopyRows];  // 16-byte units; -1 = no row
+  if (*p.err) return;  // the same value for every thread: written by the validation launch
   const int u = blockIdx.y;
   const int h = u % p.H;
   const int b = (u / p.H) % p.B;
   const int l = u / (p.H * p.B);
   const int nk = p.n_kept[u];
-  const int vec_per_row = p.d / 8;  // 8 bf16 per 16 bytes
-  const int j0 = blockIdx.x * rows_per_cta;
-  for (int i = threadIdx.x; i < rows_per_cta * vec_per_row; i += blockDim.x) {
-    const int j = j0 + i / vec_per_row, c = i % vec_per_row;
-    if (j >= nk) continue;
-    const int slot = p.kept[static_cast<size_t>(u) * p.budget + j];
-    const int t = slot - p.pad[b];
-    const int src_blk = p.table_old[static_cast<size_t>(b) * p.max_blocks + t / p.bs];
-    const int dst_blk = p.table_new[static_cast<size_t>(b) * p.max_blocks + j / p.bs];
-    const size_t src = ((((static_cast<size_t>(l) * p.n_blocks + src_blk) * p.H + h) * p.bs +
-                         t % p.bs) * p.d) / 8 + c;
-    const size_t dst = ((((static_cast<size_t>(l) * p.n_blocks + dst_blk) * p.H + h) * p.bs +
-                         j % p.bs) * p.d) / 8 + c;
-    reinterpret_cast<uint4*>(p.k_pool)[dst] = reinterpret_cast<const uint4*>(p.k_pool)[src];
-    reinterpret_cast<uint4*>(p.v_pool)[dst] = reinterpret_cast<const uint4*>(p.v_pool)[src];
-    if (c == 0)
-      p.credit_out[static_cast<size_t>(u) * p.budget + j] =
-          p.credit_post[static_cast<size_t>(u) * p.T + slot];
+  const int j0 = blockIdx.x * kCopyRows;
+  const int rows = min(kCopyRows, p.budget - j0);
+  for (int r = threadIdx.x; r < rows; r += kCopyThreads) {
+    const int j = j0 + r;
+    const size_t cj = static_cast<size_t>(u) * p.budget + j;
+    if (j < nk) {
+      const int slot = p.kept[cj];
+      const int t = slot - p.pad[b];
+      const int src_blk = p.table_old[static_cast<size_t>(b) * p.max_blocks + t / p.bs];
+      const int dst_blk = p.table_new[static_cast<size_t>(b) * p.max_blocks + j / p.bs];
+      s_src[r] = static_cast<long long>(
+                     ((static_cast<size_t>(l) * p.n_blocks + src_blk) * p.H + h) * p.bs + t % p.bs)
+                 << vpr_log2;
+      s_dst[r] = static_cast<long long>(
+                     ((static_cast<size_t>(l) * p.n_blocks + dst_blk) * p.H + h) * p.bs + j % p.bs)
+                 << vpr_log2;
+      p.credit_out[cj] = p.credit_post[static_cast<size_t>(u) * p.T + slot];
+    } else {
+      s_src[r] = -1;
+      p.credit_out[cj] = 0.f;  // slots past n_kept are zero, as in the dense compaction
+    }
   }
-  // credit slots past n_kept are zero, as in the dense compaction
-  for (int j = j0 + threadIdx.x; j < min(j0 + rows_per_cta, p.budget); j += blockDim.x)
-    if (j >= nk) p.credit_out[static_cast<size_t>(u) * p.budget + j] = 0.f;
+  __syncthreads();
+  const uint4* kin = reinterpret_cast<const uint4*>(p.k_pool);
+  const uint4* vin = reinterpret_cast<const uint4*>(p.v_pool);
+  uint4* kout = reinterpret_cast<uint4*>(p.k_pool);
+  uint4* vout = reinterpret_cast<uint4*>(p.v_pool);
+  const int vmask = (1 << vpr_log2) - 1;
+  const int total = rows << vpr_log2;
+  for (int x0 = threadIdx.x; x0 < total; x0 += kCopyThreads * kCopyUnroll) {
+    uint4 kv[kCopyUnroll], vv[kCopyUnroll];
+#pragma unroll
+    for (int i = 0; i < kCopyUnroll; ++i) {
+      const int x = x0 + i * kCopyThreads;
+      const long long src = x < total ? s_src[x >> vpr_log2] : -1;
+      if (src >= 0) {
+        kv[i] = kin[src + (x & vmask)];
+        vv[i] = vin[src + (x & vmask)];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kCopyUnroll; ++i) {
+      const int x = x0 + i * kCopyThreads;
+      if (x < total && s_src[x >> vpr_log2] >= 0) {
+        const long long dst = s_dst[x >> vpr_log2] + (x & vmask);
+        kout[dst] = kv[i];
+        vout[dst] = vv[i];
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kScanThreads) paged_free_kernel(PagedParams p) {
@@ -234,9 +273,8 @@ cudaError_t launch_compact_paged(const kvc_handle* h, const PagedArgs& a, cudaSt
   if (e != cudaSuccess) return e;
   paged_validate_kernel<<<U, 128, 0, s>>>(p);
   paged_alloc_kernel<<<1, kScanThreads, 0, s>>>(p);
-  const int rows = 32;
-  dim3 grid((p.budget + rows - 1) / rows, U);
-  paged_copy_kernel<<<grid, 256, 0, s>>>(p, rows);
+  dim3 grid((p.budget + kCopyRows - 1) / kCopyRows, U);
+  paged_copy_kernel<<<grid, kCopyThreads, 0, s>>>(p, p.d == 64 ? 3 : 4);  // d / 8 vectors per row
   paged_free_kernel<<<1, kScanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

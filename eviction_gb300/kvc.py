@@ -20,7 +20,7 @@ ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_si
                 "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
                 "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
                 "kvc_profile_read", "kvc_mass_noalloc", "kvc_refresh_decision",
-                "kvc_compact_paged", "kvc_redundancy_score")
+                "kvc_compact_paged", "kvc_redundancy_score", "kvc_wait_self_test")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -142,6 +142,7 @@ def load_library():
     L.kvc_compact_paged.argtypes = [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P,
                                     _P, _P, _P]
     L.kvc_redundancy_score.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P]
+    L.kvc_wait_self_test.argtypes = [_P, _P]
     L.kvc_status_string.argtypes = [_I]
     L.kvc_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -319,6 +320,12 @@ class Handle:
             _dev(free_list, torch.int32, "free_list"), _dev(free_top, torch.int32, "free_top"),
             _stream_ptr(stream))
         self._check(rc, "kvc_compact_paged")
+
+    def wait_self_test(self, stream=None):
+        """kvc_wait_self_test: a bounded wait that runs out on purpose (about
+        2 s); afterwards device_status() reports KVC_STATUS_WAIT_TIMEOUT."""
+        self._check(load_library().kvc_wait_self_test(self._h, _stream_ptr(stream)),
+                    "kvc_wait_self_test")
 
     def device_status(self, stream=None) -> int:
         bits = ctypes.c_uint32(0)

@@ -253,6 +253,16 @@ int kvc_compact_paged(kvc_handle* h, uint16_t* k_pool, uint16_t* v_pool, int n_b
 int kvc_refresh_decision(kvc_handle* h, const uint16_t* q, float* q_ref, float threshold,
                          int32_t* flag, float* sim, void* stream);
 
+/* ---- failure-path self-test -------------------------------------------
+ * No counterpart in the pages: a check of the library's own failure path.
+ * Launches one thread that waits, through the same bounded mbarrier wait the
+ * pipelined kernels use, on a barrier that nothing completes.  The wait gives
+ * up after its limit (about 2 s), sets KVC_STATUS_WAIT_TIMEOUT in the device
+ * status word and the kernel returns normally: nothing traps or hangs and the
+ * CUDA context stays usable.  kvc_get_device_status then reports the bit (and
+ * clears it).  Asynchronous on `stream`. */
+int kvc_wait_self_test(kvc_handle* h, void* stream);
+
 /* ---- tracing -------------------------------------------------------------
  * While enabled, every entry point records a CUDA event on its stream after
  * each kernel it launches (and one before the first), so that the time of each
