@@ -1,6 +1,7 @@
 // kvc_api.cu -- host side of the C ABI declared in include/kvc.h: argument
 // validation, the handle and its workspace, and the stage / event entry points
 // (each a fixed sequence of kernel launches on the caller's stream).
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -202,6 +203,65 @@ int run_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v, const float
   return KVC_OK;
 }
 
+// Steps 1-6 on validated pointers, intermediates in the workspace.
+int run_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_t* v, int T,
+              const int32_t* pad, const int32_t* n_carry, const float* credit_in,
+              uint16_t* k_out, uint16_t* v_out, float* credit_out, int32_t* kept_idx,
+              int32_t* n_kept, cudaStream_t s) {
+  const kvc::Workspace& w = h->ws;
+  int rc = run_mass(h, q, k, T, pad, n_carry, credit_in, w.credit_post, w.mass, w.score, s);
+  if (rc) return rc;
+  rc = run_segment_quota(h, w.mass, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, s);
+  if (rc) return rc;
+  if (h->cfg.redundancy_sigma > 0.f) {  // the selection score, in place
+    rc = run_redundancy(h, k, w.score, T, pad, w.score, nullptr, s);
+    if (rc) return rc;
+  }
+  rc = run_select(h, w.score, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, kept_idx,
+                  n_kept, s);
+  if (rc) return rc;
+  return run_compact(h, k, v, w.credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out, s);
+}
+
+int gcd_int(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+void destroy_host_io(kvc::HostIO& io) {
+  if (io.in) cudaStreamDestroy(io.in);
+  if (io.start) cudaEventDestroy(io.start);
+  for (int j = 0; j < 2; ++j) {
+    if (io.out[j]) cudaStreamDestroy(io.out[j]);
+    if (io.end[j]) cudaEventDestroy(io.end[j]);
+  }
+  for (int i = 0; i < kvc::kMaxHostStages; ++i) {
+    if (io.landed[i]) cudaEventDestroy(io.landed[i]);
+    if (io.done[i]) cudaEventDestroy(io.done[i]);
+  }
+  io = kvc::HostIO{};
+}
+
+bool create_host_io(kvc::HostIO& io) {
+  bool ok = cudaStreamCreateWithFlags(&io.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&io.start, cudaEventDisableTiming) == cudaSuccess;
+  for (int j = 0; ok && j < 2; ++j)
+    ok = cudaStreamCreateWithFlags(&io.out[j], cudaStreamNonBlocking) == cudaSuccess &&
+         cudaEventCreateWithFlags(&io.end[j], cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; ok && i < kvc::kMaxHostStages; ++i)
+    ok = cudaEventCreateWithFlags(&io.landed[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&io.done[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    destroy_host_io(io);
+  }
+  return ok;
+}
+
 }  // namespace
 
 extern "C" {
@@ -340,6 +400,11 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
   w.quota = reinterpret_cast<int32_t*>(p + o_q);
   w.n_seg = reinterpret_cast<int32_t*>(p + o_ns);
   w.status = reinterpret_cast<uint32_t*>(p + o_st);
+  if (!create_host_io(h->io)) {
+    cudaFree(base);
+    delete h;
+    return KVC_ERR_CUDA;
+  }
   *out = h;
   return KVC_OK;
 }
@@ -355,6 +420,7 @@ void kvc_destroy(kvc_handle* h) {
     cudaEventDestroy(m.end);
   }
   for (cudaEvent_t e : h->prof.pool) cudaEventDestroy(e);
+  destroy_host_io(h->io);
   delete h;
 }
 
@@ -534,20 +600,109 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_
   KVC_REQUIRE_PTR(credit_out);
   KVC_REQUIRE_PTR(kept_idx);
   KVC_REQUIRE_PTR(n_kept);
-  const kvc::Workspace& w = h->ws;
+  return run_event(h, q, k, v, T, pad, n_carry, credit_in, k_out, v_out, credit_out, kept_idx,
+                   n_kept, static_cast<cudaStream_t>(stream));
+}
+
+int kvc_event_host(kvc_handle* h, const kvc_host_buffers* io, int T, int layers_per_stage,
+                   void* stream) {
+  if (!h || !io) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  if (layers_per_stage < 1) return fail(h, KVC_ERR_ARG, "layers_per_stage must be >= 1");
+  if (!io->q_host || !io->k_host || !io->v_host || !io->pad_host || !io->n_carry_host ||
+      !io->credit_host || !io->k_out_host || !io->v_out_host || !io->credit_out_host ||
+      !io->kept_idx_host || !io->n_kept_host)
+    return fail(h, KVC_ERR_ARG, "null host pointer");
+  KVC_REQUIRE_PTR(io->q_dev);
+  KVC_REQUIRE_PTR(io->k_dev);
+  KVC_REQUIRE_PTR(io->v_dev);
+  KVC_REQUIRE_PTR(io->pad_dev);
+  KVC_REQUIRE_PTR(io->n_carry_dev);
+  KVC_REQUIRE_PTR(io->credit_dev);
+  KVC_REQUIRE_PTR(io->k_out_dev);
+  KVC_REQUIRE_PTR(io->v_out_dev);
+  KVC_REQUIRE_PTR(io->credit_out_dev);
+  KVC_REQUIRE_PTR(io->kept_idx_dev);
+  KVC_REQUIRE_PTR(io->n_kept_dev);
+  if (!h->io.in) return fail(h, KVC_ERR_CUDA, "the handle has no copy streams");
+  const kvc::Dims full = h->dims;
+  const int L = full.L, BH = full.B * full.H, K = h->cfg.budget, d = full.d;
+  // Slab offsets are multiples of B*H*4 bytes at least (n_kept): a group of nl
+  // layers keeps every slab 16-byte aligned when nl*B*H is a multiple of 4.
+  const int m = 4 / gcd_int(BH, 4);
+  int nl = ((std::min(layers_per_stage, L) + m - 1) / m) * m;
+  while ((L + nl - 1) / nl > kvc::kMaxHostStages) nl += m;
+  if (nl > L) nl = L;
+  const size_t q_l = static_cast<size_t>(BH) * full.R * d;  // elements per layer
+  const size_t kv_l = static_cast<size_t>(BH) * T * d;
+  const size_t c_l = static_cast<size_t>(BH) * T;
+  const size_t ko_l = static_cast<size_t>(BH) * K * d;
+  const size_t co_l = static_cast<size_t>(BH) * K;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = run_mass(h, q, k, T, pad, n_carry, credit_in, w.credit_post, w.mass, w.score, s);
-  if (rc) return rc;
-  rc = run_segment_quota(h, w.mass, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, s);
-  if (rc) return rc;
-  if (h->cfg.redundancy_sigma > 0.f) {  // the selection score, in place
-    rc = run_redundancy(h, k, w.score, T, pad, w.score, nullptr, s);
+  kvc::HostIO& x = h->io;
+  auto h2d = [&](void* dst, const void* src, size_t bytes) {
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, x.in);
+  };
+  // device -> host: each slab in two halves, one per output stream
+  auto d2h = [&](void* dst, const void* src, size_t bytes) {
+    const size_t first = (bytes / 2) & ~size_t(15);
+    cudaError_t r = cudaMemcpyAsync(dst, src, first, cudaMemcpyDeviceToHost, x.out[0]);
+    if (r == cudaSuccess && bytes > first)
+      r = cudaMemcpyAsync(static_cast<char*>(dst) + first, static_cast<const char*>(src) + first,
+                          bytes - first, cudaMemcpyDeviceToHost, x.out[1]);
+    return r;
+  };
+  // the copies start after the work already queued on `stream`
+  cudaError_t e = cudaEventRecord(x.start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(x.in, x.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(x.out[0], x.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(x.out[1], x.start, 0);
+  if (e == cudaSuccess) e = h2d(io->pad_dev, io->pad_host, static_cast<size_t>(full.B) * 4);
+  if (e == cudaSuccess)
+    e = h2d(io->n_carry_dev, io->n_carry_host, static_cast<size_t>(full.B) * 4);
+  if (e != cudaSuccess) return cuda_fail(h, e, "host event: setup");
+  int g = 0;
+  for (int l0 = 0; l0 < L; l0 += nl, ++g) {
+    const int n = std::min(nl, L - l0);
+    const size_t lq = l0 * q_l, lkv = l0 * kv_l, lc = l0 * c_l, lko = l0 * ko_l, lco = l0 * co_l;
+    e = h2d(io->q_dev + lq, io->q_host + lq, n * q_l * 2);
+    if (e == cudaSuccess) e = h2d(io->k_dev + lkv, io->k_host + lkv, n * kv_l * 2);
+    if (e == cudaSuccess) e = h2d(io->v_dev + lkv, io->v_host + lkv, n * kv_l * 2);
+    if (e == cudaSuccess) e = h2d(io->credit_dev + lc, io->credit_host + lc, n * c_l * 4);
+    if (e == cudaSuccess) e = cudaEventRecord(x.landed[g], x.in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, x.landed[g], 0);
+    if (e != cudaSuccess) return cuda_fail(h, e, "host event: inputs");
+    // the event on layers [l0, l0 + n): the same kernels on a handle view of n layers
+    h->dims.L = n;
+    h->dims.U = n * BH;
+    rc = run_event(h, io->q_dev + lq, io->k_dev + lkv, io->v_dev + lkv, T, io->pad_dev,
+                   io->n_carry_dev, io->credit_dev + lc, io->k_out_dev + lko,
+                   io->v_out_dev + lko, io->credit_out_dev + lco, io->kept_idx_dev + lco,
+                   io->n_kept_dev + static_cast<size_t>(l0) * BH, s);
+    h->dims = full;
     if (rc) return rc;
+    e = cudaEventRecord(x.done[g], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(x.out[0], x.done[g], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(x.out[1], x.done[g], 0);
+    if (e == cudaSuccess) e = d2h(io->k_out_host + lko, io->k_out_dev + lko, n * ko_l * 2);
+    if (e == cudaSuccess) e = d2h(io->v_out_host + lko, io->v_out_dev + lko, n * ko_l * 2);
+    if (e == cudaSuccess)
+      e = d2h(io->credit_out_host + lco, io->credit_out_dev + lco, n * co_l * 4);
+    if (e == cudaSuccess)
+      e = d2h(io->kept_idx_host + lco, io->kept_idx_dev + lco, n * co_l * 4);
+    if (e == cudaSuccess)
+      e = d2h(io->n_kept_host + static_cast<size_t>(l0) * BH,
+              io->n_kept_dev + static_cast<size_t>(l0) * BH, static_cast<size_t>(n) * BH * 4);
+    if (e != cudaSuccess) return cuda_fail(h, e, "host event: outputs");
   }
-  rc = run_select(h, w.score, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, kept_idx,
-                  n_kept, s);
-  if (rc) return rc;
-  return run_compact(h, k, v, w.credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out, s);
+  // `stream` completes only after the last host copy
+  for (int j = 0; j < 2 && e == cudaSuccess; ++j) {
+    e = cudaEventRecord(x.end[j], x.out[j]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, x.end[j], 0);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "host event: end");
+  return KVC_OK;
 }
 
 int kvc_profile(kvc_handle* h, int enable) {

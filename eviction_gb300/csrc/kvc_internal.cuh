@@ -71,6 +71,17 @@ struct Profiler {
 
 }  // namespace kvc
 
+namespace kvc {
+// Copy streams and events of kvc_event_host (created with the handle).
+constexpr int kMaxHostStages = 64;
+struct HostIO {
+  cudaStream_t in = nullptr, out[2] = {nullptr, nullptr};  // device -> host on two streams:
+  cudaEvent_t start = nullptr, end[2] = {nullptr, nullptr};  // one alone reaches ~1/3 of the link
+  cudaEvent_t landed[kMaxHostStages] = {};  // a stage's inputs are on the device
+  cudaEvent_t done[kMaxHostStages] = {};    // a stage's outputs are written
+};
+}  // namespace kvc
+
 struct kvc_handle {
   kvc_config cfg;
   kvc::Dims dims;
@@ -79,6 +90,7 @@ struct kvc_handle {
   int num_sms = 0;
   std::string last_error;
   kvc::Profiler prof;
+  kvc::HostIO io;
 };
 
 namespace kvc {

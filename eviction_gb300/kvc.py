@@ -20,7 +20,8 @@ ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_si
                 "kvc_mass", "kvc_segment_quota", "kvc_select", "kvc_compact", "kvc_event",
                 "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
                 "kvc_profile_read", "kvc_mass_noalloc", "kvc_refresh_decision",
-                "kvc_compact_paged", "kvc_redundancy_score", "kvc_wait_self_test")
+                "kvc_compact_paged", "kvc_redundancy_score", "kvc_wait_self_test",
+                "kvc_event_host")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -103,6 +104,19 @@ class Config:
         return self.n_layers * self.batch * self.n_kv_heads
 
 
+_HOST_BUFFER_FIELDS = ("q", "k", "v", "pad", "n_carry", "credit")
+_HOST_OUT_FIELDS = ("k_out", "v_out", "credit_out", "kept_idx", "n_kept")
+
+
+class _HostBuffers(ctypes.Structure):
+    """kvc_host_buffers: (host, device) pointer pairs, inputs then outputs
+    (outputs are listed device first, as in the C struct)."""
+    _fields_ = ([(f"{k}_{side}", ctypes.c_void_p) for k in _HOST_BUFFER_FIELDS
+                 for side in ("host", "dev")] +
+                [(f"{k}_{side}", ctypes.c_void_p) for k in _HOST_OUT_FIELDS
+                 for side in ("dev", "host")])
+
+
 _lib = None
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -143,6 +157,7 @@ def load_library():
                                     _P, _P, _P]
     L.kvc_redundancy_score.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P]
     L.kvc_wait_self_test.argtypes = [_P, _P]
+    L.kvc_event_host.argtypes = [_P, ctypes.POINTER(_HostBuffers), _I, _I, _P]
     L.kvc_status_string.argtypes = [_I]
     L.kvc_status_string.restype = ctypes.c_char_p
     for name in ENTRY_POINTS:
@@ -371,6 +386,40 @@ class Handle:
             for key in ("k_out", "v_out", "credit_out", "kept_idx", "n_kept"):
                 host_out[key].copy_(dev_out[key], non_blocking=True)
                 d2h += dev_out[key].numel() * dev_out[key].element_size()
+        return h2d, d2h
+
+    def event_from_host(self, host_in: dict, dev_in: dict, host_out: dict, dev_out: dict,
+                        T: int, layers_per_stage: int = 4, stream=None):
+        """kvc_event_host: the event from pinned host buffers, pipelined over
+        groups of layers (host -> device copies of the next group and device ->
+        host copies of the previous one overlap the current group's event).
+        host_in / dev_in: q, k, v, pad, n_carry, credit; host_out / dev_out:
+        k_out, v_out, credit_out, kept_idx, n_kept.  Returns the bytes moved
+        each way; the work is complete once `stream` is."""
+        import torch
+        hb = _HostBuffers()
+        dtypes = dict(q=torch.bfloat16, k=torch.bfloat16, v=torch.bfloat16, pad=torch.int32,
+                      n_carry=torch.int32, credit=torch.float32, k_out=torch.bfloat16,
+                      v_out=torch.bfloat16, credit_out=torch.float32, kept_idx=torch.int32,
+                      n_kept=torch.int32)
+        h2d = d2h = 0
+        for key in _HOST_BUFFER_FIELDS + _HOST_OUT_FIELDS:
+            hs = host_in[key] if key in host_in else host_out[key]
+            ds = dev_in[key] if key in dev_in else dev_out[key]
+            if hs.is_cuda or hs.dtype != dtypes[key] or not hs.is_contiguous():
+                raise ValueError(f"{key}: host tensor must be a contiguous CPU {dtypes[key]}")
+            if hs.numel() != ds.numel():
+                raise ValueError(f"{key}: host and device sizes differ")
+            setattr(hb, f"{key}_host", hs.data_ptr())
+            setattr(hb, f"{key}_dev", _dev(ds, dtypes[key], key).value)
+            nbytes = hs.numel() * hs.element_size()
+            if key in _HOST_BUFFER_FIELDS:
+                h2d += nbytes
+            else:
+                d2h += nbytes
+        rc = load_library().kvc_event_host(self._h, ctypes.byref(hb), T, int(layers_per_stage),
+                                           _stream_ptr(stream))
+        self._check(rc, "kvc_event_host")
         return h2d, d2h
 
     # -- allocation conveniences (torch allocates; the library never does) ---

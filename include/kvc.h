@@ -200,6 +200,36 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
               uint16_t* k_out, uint16_t* v_out, float* credit_out,
               int32_t* kept_idx, int32_t* n_kept, void* stream);
 
+/* The whole event from host buffers, pipelined over groups of layers.
+ * No counterpart in the pages: the deployment path when the caches live in
+ * host memory.  The layer-major layout makes each group of layers one
+ * contiguous slab of every tensor; the slabs of group g+1 are copied host ->
+ * device on one of the handle's copy streams while group g's event runs on
+ * `stream`, and group g-1's outputs go device -> host on two others (each
+ * slab in two halves: one device -> host stream alone moves far less).  Every
+ * pointer is as for kvc_event (device ones 16-byte aligned); host buffers
+ * should be page-locked for the copies to overlap.  The device input and
+ * output buffers are the caller's, full size ([L][...]).  layers_per_stage >= 1
+ * is rounded up so that every slab starts on a 16-byte boundary (at most 64
+ * stages).  When the call returns the work is queued; everything, the last
+ * host copy included, is complete once `stream` is.  Uses cudaMemcpyAsync. */
+typedef struct {
+  const uint16_t* q_host;      uint16_t* q_dev;       /* [L][B][H*G][W][d] */
+  const uint16_t* k_host;      uint16_t* k_dev;       /* [L][B][H][T][d]   */
+  const uint16_t* v_host;      uint16_t* v_dev;
+  const int32_t* pad_host;     int32_t* pad_dev;      /* [B] */
+  const int32_t* n_carry_host; int32_t* n_carry_dev;  /* [B] */
+  const float* credit_host;    float* credit_dev;     /* [L][B][H][T] */
+  uint16_t* k_out_dev;         uint16_t* k_out_host;  /* [L][B][H][budget][d] */
+  uint16_t* v_out_dev;         uint16_t* v_out_host;
+  float* credit_out_dev;       float* credit_out_host;  /* [L][B][H][budget] */
+  int32_t* kept_idx_dev;       int32_t* kept_idx_host;  /* [L][B][H][budget] */
+  int32_t* n_kept_dev;         int32_t* n_kept_host;    /* [L][B][H] */
+} kvc_host_buffers;
+
+int kvc_event_host(kvc_handle* h, const kvc_host_buffers* io, int T, int layers_per_stage,
+                   void* stream);
+
 /* Step 6 into a paged KV pool ("Adaptive Mass-Segmented KV Compression for
  * Long-Form Reasoning", Appendix E): new blocks are taken from a free stack,
  * each head's kept rows are copied from their original positions into the
