@@ -12,9 +12,11 @@
 // The base score ("RefreshKV: ...", A2: max pooling of neighbouring attention
 // scores; A6: kernel 7) is the filled usage max-pooled over valid neighbours.
 //
-// The unit's data (a few KB per array) stays in L1/L2 between the sweeps; each
-// sweep is a strided pass plus one block reduction (fixed order, so repeated
-// runs give identical bits).
+// Units up to 4096 slots take one pass with the filled usage in shared memory
+// and per-slot values in registers; longer ones sweep global memory (the
+// unit's data stays in L1/L2 between sweeps).  Every sum is a strided
+// per-thread pass plus one fixed-order block reduction, so repeated runs give
+// identical bits.
 #include <cmath>
 
 #include "kvc_internal.cuh"
@@ -165,6 +167,127 @@ __global__ void __launch_bounds__(kThreads)
   for (int i = pad + threadIdx.x; i < T; i += kThreads) mass[i] = mass[i] / mix_total;
 }
 
+// Units of up to kSmemT slots: one pass.  The filled usage of the unit sits in
+// shared memory (the pooling windows read it there), each thread keeps its
+// slots' values in registers across the normalisations, and score, mass and
+// credit are written once.  The arithmetic and the summation order (per thread
+// over its slots, then block_sum) are those of the general kernel below.
+constexpr int kSmemT = 4096;
+
+template <int kEpt>  // slots per thread: T <= kEpt * kThreads
+__global__ void __launch_bounds__(kThreads)
+    mass_post_smem_kernel(PostParams p) {
+  __shared__ float red[kThreads / 32 + 1];
+  __shared__ float a[kEpt * kThreads];
+  const int u = blockIdx.x;
+  const int b = (u / p.H) % p.B;
+  const int T = p.T;
+  const int pad = min(max(p.pad[b], 0), T);
+  const size_t base = static_cast<size_t>(u) * T;
+  float* mass = p.mass + base;
+  float* score = p.score + base;
+  float* cpost = p.credit_post + base;
+  const float* cin = p.credit_in + base;
+  const float* usage = p.usage + base;
+
+  if (pad >= T) {
+    for (int i = threadIdx.x; i < T; i += kThreads) {
+      mass[i] = 0.f;
+      score[i] = -INFINITY;
+      cpost[i] = 0.f;
+    }
+    return;
+  }
+  const int n_carry = min(max(p.n_carry[b], 0), T - pad);
+  // this thread's credit-in values, loaded early (used after two reductions)
+  float cprior[kEpt];
+#pragma unroll
+  for (int k = 0; k < kEpt; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    cprior[k] = (i >= pad && i < pad + n_carry) ? cin[i] : 0.f;
+  }
+
+  float pm = 0.f;
+  for (int r = threadIdx.x; r < p.R; r += kThreads)
+    pm = fmaxf(pm, p.pmax[static_cast<size_t>(u) * p.Rp + r]);
+  const float fill = block_max(pm, red);
+
+  const int j_lo = max(0, pad - (T - p.W));
+#pragma unroll
+  for (int k = 0; k < kEpt; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    if (i < T) {
+      const int unseen = max(0, min(p.W, i - T + p.W) - j_lo) * p.G;
+      a[i] = i >= pad ? usage[i] + fill * static_cast<float>(unseen) : 0.f;
+    }
+  }
+  __syncthreads();
+
+  const int ra = p.avg_pool / 2, rm = p.max_pool / 2;
+  const float inv_k = 1.0f / static_cast<float>(p.avg_pool);
+  float up[kEpt];  // max(avg pool, 0) + eps
+  float tot = 0.f;
+#pragma unroll
+  for (int k = 0; k < kEpt; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    up[k] = 0.f;
+    if (i >= T) continue;
+    if (i < pad) {
+      score[i] = -INFINITY;
+      continue;
+    }
+    float mx = -INFINITY;
+    for (int t = max(pad, i - rm); t <= min(T - 1, i + rm); ++t) mx = fmaxf(mx, a[t]);
+    score[i] = mx;
+    float sm = 0.f;
+    for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) sm += a[t];
+    up[k] = fmaxf(sm * inv_k, 0.f) + p.eps;
+    tot += up[k];
+  }
+  const float total1 = block_sum(tot, red);
+
+  const float lam = p.lambda;
+  float ctot = 0.f;
+#pragma unroll
+  for (int k = 0; k < kEpt; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    if (i < pad || i >= T) continue;
+    const float m = up[k] / total1;
+    const float prior = (i < pad + n_carry) ? cprior[k] : m;
+    const float c = lam * prior + (1.0f - lam) * m;
+    up[k] = m;
+    cprior[k] = c;
+    ctot += c;
+  }
+  const float c_total = block_sum(ctot, red);
+
+  const float beta = p.beta;
+  float mtot = 0.f;
+#pragma unroll
+  for (int k = 0; k < kEpt; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    if (i < pad || i >= T) continue;
+    const float m = up[k];
+    const float cn = (c_total > 0.f) ? cprior[k] / c_total : m;
+    const float mix = beta * m + (1.0f - beta) * cn;
+    up[k] = mix;
+    mtot += mix;
+  }
+  const float mix_total = block_sum(mtot, red);
+#pragma unroll
+  for (int k = 0; k < kEpt; ++k) {
+    const int i = threadIdx.x + k * kThreads;
+    if (i >= T) continue;
+    if (i < pad) {
+      mass[i] = 0.f;
+      cpost[i] = 0.f;
+    } else {
+      mass[i] = up[k] / mix_total;
+      cpost[i] = cprior[k];
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
@@ -193,7 +316,14 @@ cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
   p.credit_post = credit_post;
   p.mass = mass;
   p.score = score;
-  mass_post_kernel<<<dm.U, kThreads, 0, s>>>(p);
+  if (T <= 4 * kThreads)
+    mass_post_smem_kernel<4><<<dm.U, kThreads, 0, s>>>(p);
+  else if (T <= 8 * kThreads)
+    mass_post_smem_kernel<8><<<dm.U, kThreads, 0, s>>>(p);
+  else if (T <= kSmemT)
+    mass_post_smem_kernel<kSmemT / kThreads><<<dm.U, kThreads, 0, s>>>(p);
+  else
+    mass_post_kernel<<<dm.U, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
