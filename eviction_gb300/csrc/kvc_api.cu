@@ -632,7 +632,7 @@ int kvc_event_host(kvc_handle* h, const kvc_host_buffers* io, int T, int layers_
   // layers keeps every slab 16-byte aligned when nl*B*H is a multiple of 4.
   const int m = 4 / gcd_int(BH, 4);
   int nl = ((std::min(layers_per_stage, L) + m - 1) / m) * m;
-  while ((L + nl - 1) / nl > kvc::kMaxHostStages) nl += m;
+  while ((L + nl - 1) / nl + 1 > kvc::kMaxHostStages) nl += m;
   if (nl > L) nl = L;
   const size_t q_l = static_cast<size_t>(BH) * full.R * d;  // elements per layer
   const size_t kv_l = static_cast<size_t>(BH) * T * d;
@@ -663,8 +663,19 @@ int kvc_event_host(kvc_handle* h, const kvc_host_buffers* io, int T, int layers_
     e = h2d(io->n_carry_dev, io->n_carry_host, static_cast<size_t>(full.B) * 4);
   if (e != cudaSuccess) return cuda_fail(h, e, "host event: setup");
   int g = 0;
-  for (int l0 = 0; l0 < L; l0 += nl, ++g) {
-    const int n = std::min(nl, L - l0);
+  // Stages of nl layers, except at the end: the host -> device copies are the
+  // critical path, and what follows the last of them (that stage's event and
+  // its device -> host copies) is shortest when the last stage is small.  So
+  // the last stage keeps 1..m layers and the one before it the rest; every
+  // stage but the last is a multiple of m layers, so every stage starts aligned.
+  auto stage_layers = [&](int l0) {
+    const int left = L - l0;
+    if (left <= m) return left;
+    const int last = (left - 1) % m + 1;
+    return left - last <= nl ? left - last : nl;
+  };
+  for (int l0 = 0, n = 0; l0 < L; l0 += n, ++g) {
+    n = stage_layers(l0);
     const size_t lq = l0 * q_l, lkv = l0 * kv_l, lc = l0 * c_l, lko = l0 * ko_l, lco = l0 * co_l;
     e = h2d(io->q_dev + lq, io->q_host + lq, n * q_l * 2);
     if (e == cudaSuccess) e = h2d(io->k_dev + lkv, io->k_host + lkv, n * kv_l * 2);

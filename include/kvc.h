@@ -211,7 +211,8 @@ int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
  * should be page-locked for the copies to overlap.  The device input and
  * output buffers are the caller's, full size ([L][...]).  layers_per_stage >= 1
  * is rounded up so that every slab starts on a 16-byte boundary (at most 64
- * stages).  When the call returns the work is queued; everything, the last
+ * stages); the last stage is kept as small as that allows, since its event and
+ * copies back are all that follows the last host -> device copy.  When the call returns the work is queued; everything, the last
  * host copy included, is complete once `stream` is.  Uses cudaMemcpyAsync. */
 typedef struct {
   const uint16_t* q_host;      uint16_t* q_dev;       /* [L][B][H*G][W][d] */
