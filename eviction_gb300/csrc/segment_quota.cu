@@ -28,7 +28,7 @@
 namespace kvc {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 128;  // per-unit latency chains: more CTAs in flight beat wider ones
 constexpr int kMaxK = 1024;  // thresholds: delta >= 1/1024
 constexpr int kFastSegs = 256;  // segment count up to which the quota correction ranks directly
 
