@@ -1,7 +1,8 @@
 // redundancy.cu -- SkipKV key-redundancy score mixed into the selection score.
 //
-// "SkipKV: ...", A2 token redundancy score (after R-KV) and the final eviction
-// score: per KV head, r_i = the mean cosine similarity of key i to the other
+// "SkipKV: Selective Skipping of KV Generation and Storage for Efficient
+// Inference with Large Reasoning Models", A2 Method details, 4.1: the token
+// redundancy score (after R-KV) and the final eviction score: per KV head, r_i = the mean cosine similarity of key i to the other
 // valid keys, R = softmax of r over the valid slots, I = score / (sum of the
 // score over the valid slots), and selection runs on f = sigma*I - (1-sigma)*R
 // (more redundant -> evicted earlier).  Padding slots never count and get

@@ -21,7 +21,7 @@
  * owned, C-contiguous, 16-byte aligned, with the layer dimension outermost):
  *   q       [L][B][H*G][W][d]  bf16 (raw 16-bit patterns, uint16_t);
  *                              query head h*G+g belongs to KV head h
- *                              ("SkipKV: ...", A2 token importance: g(i)=floor(i/n))
+ *                              (SkipKV, A2 Method details, 4.1 token importance: g(i)=floor(i/n))
  *   k, v    [L][B][H][T][d]    bf16; slot t of a sequence with left padding
  *                              pad[b] is valid iff t >= pad[b]
  *   credit  [L][B][H][T]       fp32 EMA credit (Key design 1)
@@ -118,7 +118,7 @@ typedef struct {
                         segment mass (same minimums, rounding, correction)  */
   int global_topk;   /* 1: one segment over all valid slots, quota = budget:
                         per-head top-k on the score plus the must-keep set  */
-  /* Second base score ("SkipKV: ...", A2 token redundancy score, after R-KV):
+  /* Second base score (SkipKV, A2 Method details, 4.1 token redundancy score, after R-KV):
    * sigma in (0, 1] selects on sigma*I - (1-sigma)*R instead of the score
    * (see kvc_redundancy_score); 0 = off.  Segments and quotas stay on the
    * attention mass.                                                         */
@@ -170,7 +170,9 @@ int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
                 const int32_t* n_kept, uint16_t* k_out, uint16_t* v_out,
                 float* credit_out, void* stream);
 
-/* Second base score ("SkipKV: ...", A2 token redundancy score after R-KV, and
+/* Second base score ("SkipKV: Selective Skipping of KV Generation and Storage
+ * for Efficient Inference with Large Reasoning Models", A2 Method details, 4.1:
+ * the token redundancy score after R-KV, and
  * the final eviction score without its sentence term), for every unit:
  *   r_i = mean over the other valid slots j != i of cos(k_i, k_j)
  *         (a zero key has cosine 0 with every key; r = 0 below two valid slots),

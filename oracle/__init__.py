@@ -10,8 +10,9 @@ module only compiles it with gcc and marshals numpy arrays through ctypes.
 Sources: "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning"
 (Method, Key designs 1-4; the complete example), "RefreshKV: Updating Small KV
 Cache During Long-form Generation" (A2 max pooling; A6 kernel size 7) and
-"SkipKV: ..." (A2 token importance score, GQA mapping and mask; A2 token
-redundancy score and the sigma mix of the final score).
+"SkipKV: Selective Skipping of KV Generation and Storage for Efficient Inference
+with Large Reasoning Models" (A2 Method details, 4.1: token importance score, GQA
+mapping and mask; token redundancy score and the sigma mix of the final score).
 """
 from __future__ import annotations
 

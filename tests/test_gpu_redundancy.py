@@ -1,5 +1,7 @@
-"""GPU parity of the second base score ("SkipKV: ...", A2 token redundancy score
-after R-KV, and the sigma mix of the final eviction score) against the oracle.
+"""GPU parity of the second base score ("SkipKV: Selective Skipping of KV
+Generation and Storage for Efficient Inference with Large Reasoning Models", A2
+Method details, 4.1: token redundancy score after R-KV, and the sigma mix of the
+final eviction score) against the oracle.
 
 The oracle computes the pairwise definition (every cosine, fp64); the kernel
 uses sum_j cos(k_i, k_j) = k^_i . sum_j k^_j - 1 in fp32.  Tolerances follow

@@ -1,5 +1,7 @@
-"""Pins of the oracle's second base score ("SkipKV: ...", A2 token redundancy
-score after R-KV, and the sigma mix of the final eviction score): closed forms
+"""Pins of the oracle's second base score ("SkipKV: Selective Skipping of KV
+Generation and Storage for Efficient Inference with Large Reasoning Models", A2
+Method details, 4.1: token redundancy score after R-KV, and the sigma mix of the
+final eviction score): closed forms
 on keys whose cosines are known exactly (parallel, antipodal, orthogonal
 clusters at arbitrary scales), the mask, zero keys, the softmax and the
 normalised importance, and the sign of the mix seen through the selection."""
