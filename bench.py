@@ -519,12 +519,15 @@ def run_ours(args, w):
             h2d, d2h = h.event_from_host(host_in, dev_in, host_out, out, T, layers_per_stage=lps)
         f1.record(stream)
         torch.cuda.synchronize(dev)
+        # V is read in place at the kept rows (page-locked host buffer)
+        h2d += int(host_out["n_kept"].long().sum().item()) * w.head_dim * 2
         e2e_ms = f0.elapsed_time(f1) / args.e2e_steps
         e2e_ms, _ = reduce_over_ranks(e2e_ms, 0.0, dev)
         e2e = {"value": total_tokens / (e2e_ms / 1000.0), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": args.e2e_steps,
-               "path": f"kvc_event_host, pinned host buffers, {lps} layers per copy stage"}
+               "path": f"kvc_event_host, pinned host buffers, {lps} layers per copy stage; "
+                       "V read in place at the kept rows"}
         del host_in, host_out
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1)

@@ -662,6 +662,19 @@ int kvc_event_host(kvc_handle* h, const kvc_host_buffers* io, int T, int layers_
   if (e == cudaSuccess)
     e = h2d(io->n_carry_dev, io->n_carry_host, static_cast<size_t>(full.B) * 4);
   if (e != cudaSuccess) return cuda_fail(h, e, "host event: setup");
+  // V is read only at the kept rows (by the gather): when the host buffer is
+  // mapped into the device's address space, the gather reads it there and V
+  // is not copied
+  const uint16_t* v_mapped = nullptr;
+  {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, io->v_host) == cudaSuccess) {
+      if (pa.type == cudaMemoryTypeHost && pa.devicePointer)
+        v_mapped = static_cast<const uint16_t*>(pa.devicePointer);
+    } else {
+      cudaGetLastError();
+    }
+  }
   int g = 0;
   // Stages of nl layers, except at the end: the host -> device copies are the
   // critical path, and what follows the last of them (that stage's event and
@@ -679,7 +692,8 @@ int kvc_event_host(kvc_handle* h, const kvc_host_buffers* io, int T, int layers_
     const size_t lq = l0 * q_l, lkv = l0 * kv_l, lc = l0 * c_l, lko = l0 * ko_l, lco = l0 * co_l;
     e = h2d(io->q_dev + lq, io->q_host + lq, n * q_l * 2);
     if (e == cudaSuccess) e = h2d(io->k_dev + lkv, io->k_host + lkv, n * kv_l * 2);
-    if (e == cudaSuccess) e = h2d(io->v_dev + lkv, io->v_host + lkv, n * kv_l * 2);
+    if (e == cudaSuccess && !v_mapped)
+      e = h2d(io->v_dev + lkv, io->v_host + lkv, n * kv_l * 2);
     if (e == cudaSuccess) e = h2d(io->credit_dev + lc, io->credit_host + lc, n * c_l * 4);
     if (e == cudaSuccess) e = cudaEventRecord(x.landed[g], x.in);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, x.landed[g], 0);
@@ -687,8 +701,8 @@ int kvc_event_host(kvc_handle* h, const kvc_host_buffers* io, int T, int layers_
     // the event on layers [l0, l0 + n): the same kernels on a handle view of n layers
     h->dims.L = n;
     h->dims.U = n * BH;
-    rc = run_event(h, io->q_dev + lq, io->k_dev + lkv, io->v_dev + lkv, T, io->pad_dev,
-                   io->n_carry_dev, io->credit_dev + lc, io->k_out_dev + lko,
+    rc = run_event(h, io->q_dev + lq, io->k_dev + lkv,
+                   v_mapped ? v_mapped + lkv : io->v_dev + lkv, T, io->pad_dev, io->n_carry_dev, io->credit_dev + lc, io->k_out_dev + lko,
                    io->v_out_dev + lko, io->credit_out_dev + lco, io->kept_idx_dev + lco,
                    io->n_kept_dev + static_cast<size_t>(l0) * BH, s);
     h->dims = full;

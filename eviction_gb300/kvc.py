@@ -394,8 +394,10 @@ class Handle:
         groups of layers (host -> device copies of the next group and device ->
         host copies of the previous one overlap the current group's event).
         host_in / dev_in: q, k, v, pad, n_carry, credit; host_out / dev_out:
-        k_out, v_out, credit_out, kept_idx, n_kept.  Returns the bytes moved
-        each way; the work is complete once `stream` is."""
+        k_out, v_out, credit_out, kept_idx, n_kept.  Returns the bytes copied
+        each way; a page-locked V is read in place at the kept rows only (not
+        counted here: n_kept * d * 2 bytes per unit).  The work is complete
+        once `stream` is."""
         import torch
         hb = _HostBuffers()
         dtypes = dict(q=torch.bfloat16, k=torch.bfloat16, v=torch.bfloat16, pad=torch.int32,
@@ -413,6 +415,8 @@ class Handle:
             setattr(hb, f"{key}_host", hs.data_ptr())
             setattr(hb, f"{key}_dev", _dev(ds, dtypes[key], key).value)
             nbytes = hs.numel() * hs.element_size()
+            if key == "v" and hs.is_pinned():
+                continue  # read in place at the kept rows by the gather
             if key in _HOST_BUFFER_FIELDS:
                 h2d += nbytes
             else:

@@ -44,11 +44,13 @@ def test_host_pipelined_equals_device_event(n_layers, batch, heads, per_stage):
                                  layers_per_stage=per_stage, stream=stream)
     stream.synchronize()
     assert h.device_status() == 0
-    assert h2d == sum(t.numel() * t.element_size() for t in host_in.values())
+    # every input is copied except V, which the gather reads in place (pinned)
+    assert h2d == sum(t.numel() * t.element_size() for k, t in host_in.items() if k != "v")
     for k in ("k_out", "v_out", "credit_out", "kept_idx", "n_kept"):
         assert torch.equal(host_out[k], ref[k].cpu()), k
     for k in keys_in:
-        assert torch.equal(dev_in[k], g[k]), k
+        if k != "v":
+            assert torch.equal(dev_in[k], g[k]), k
 
 
 def test_host_pipelined_argument_errors():
@@ -70,3 +72,29 @@ def test_host_pipelined_argument_errors():
     h.event_from_host(host_in, dev_in, host_out, dev_out, T, layers_per_stage=1)
     torch.cuda.synchronize()
     assert h.device_status() == 0
+
+
+def test_host_pipelined_pageable_v_falls_back_to_copies():
+    """V in pageable host memory is copied like the other inputs (the gather
+    reads V in place only from page-locked, device-mapped memory)."""
+    import eviction_gb300 as kvc
+    w = wl.scaled(wl.CONFIGS["llama_ragged"], n_layers=4, batch=2, n_kv_heads=2, group=4,
+                  head_dim=128, prefill=(50, 400), generated=300, budget=256)
+    inp = wl.generate(w)
+    T = inp.T
+    g = gu.to_device(inp)
+    h = kvc.Handle(gu.config_for(w, T))
+    ref = gu.gpu_event(h, g, T)
+    keys_in = ("q", "k", "v", "pad", "n_carry", "credit")
+    host_in = {k: (g[k].cpu() if k == "v" else g[k].cpu().pin_memory()) for k in keys_in}
+    assert not host_in["v"].is_pinned()
+    dev_in = {k: torch.empty_like(g[k]) for k in keys_in}
+    dev_out = h.outputs(T)
+    host_out = {k: torch.full(v.shape, 7, dtype=v.dtype).pin_memory() for k, v in dev_out.items()}
+    h2d, _ = h.event_from_host(host_in, dev_in, host_out, dev_out, T, layers_per_stage=2)
+    torch.cuda.synchronize()
+    assert h.device_status() == 0
+    assert h2d == sum(t.numel() * t.element_size() for t in host_in.values())
+    assert torch.equal(dev_in["v"], g["v"])
+    for k in ("k_out", "v_out", "credit_out", "kept_idx", "n_kept"):
+        assert torch.equal(host_out[k], ref[k].cpu()), k
