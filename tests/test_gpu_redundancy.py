@@ -281,3 +281,26 @@ def test_event_with_sigma_end_to_end(ref):
     # sigma really changes the selection
     r0 = ref.event(gu.ref_params(ref, w), *gu.oracle_inputs(inp))
     assert not np.array_equal(r0["kept_idx"], r["kept_idx"])
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_redundancy_random_shapes(ref, seed):
+    """Seeded random small shapes (T from 1, both head sizes, units that are all
+    padding, one or two valid slots) against the oracle's pairwise definition."""
+    import eviction_gb300 as kvc
+    rng = np.random.default_rng(500 + seed)
+    d = int(rng.choice([64, 128]))
+    T = int(rng.integers(1, 3000))
+    B, H = int(rng.integers(1, 4)), int(rng.integers(1, 3))
+    pads = [int(x) for x in rng.integers(0, T + 1, B)]
+    pads[0] = [0, T, max(T - 1, 0), max(T - 2, 0)][seed % 4]
+    kb = _keys(rng, 1, B, H, T, d, pads)
+    sc = _scores(rng, 1, B, H, T, pads)
+    sigma = float(rng.choice([0.1, 0.5, 1.0]))
+    f_g, R_g, _ = _run(kvc, 1, B, H, T, d, pads, kb, sc, sigma)
+    U = B * H
+    pad_u = np.array([pads[(u // H) % B] for u in range(U)])
+    f_o, R_o, _ = ref.redundancy_score(kb.reshape(U, T, d), sc.reshape(U, T), pad_u, sigma)
+    for u in range(U):
+        _check_unit(f_g.reshape(U, T)[u], R_g.reshape(U, T)[u], f_o[u], R_o[u],
+                    sc.reshape(U, T)[u], pad_u[u], sigma)
