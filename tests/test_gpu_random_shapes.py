@@ -57,7 +57,7 @@ def _with_pads(inp, pads):
     return inp
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_shape(ref, seed):
     import eviction_gb300 as kvc
     s = _shape(seed)
