@@ -31,8 +31,10 @@
 // bulk copy), warp 1 issues tcgen05.mma, and 16 epilogue warps (warps 2-17:
 // tile slot x column half x lane quarter) drain the accumulators, 64 columns
 // at a time, releasing an accumulator once its last columns are in registers.
-// The two column halves of a row (pass 1) or slot (pass 2) are combined at
-// the end of the item.  Every wait is bounded.
+// At the end of an item the two column halves of a row (pass 1) or slot
+// (pass 2) leave their partials in shared memory and go straight on; warp 19
+// combines them and writes the results, so that the combination is not on the
+// accumulator hand-off path.  Every wait is bounded.
 #include <cmath>
 #include <cstdio>
 
@@ -43,7 +45,8 @@ namespace {
 
 constexpr int kEpiWarps = 16;                     // tile slot x column half x lane quarter
 constexpr int kLoaderWarp = 2 + kEpiWarps;        // A tiles / row constants
-constexpr int kThreads = 32 * (kLoaderWarp + 1);  // B warp, MMA warp, epilogue, loader
+constexpr int kMergeWarp = kLoaderWarp + 1;       // combines the two column halves
+constexpr int kThreads = 32 * (kMergeWarp + 1);   // B, MMA, epilogue, loader, merge
 constexpr int BM = 128;         // A-operand rows per tile (TMEM lanes)
 constexpr int BN = 256;         // B-operand rows per chunk (accumulator columns)
 constexpr int kHalf = BN / 2;   // accumulator columns per epilogue column half
@@ -51,10 +54,17 @@ constexpr int kTiles = 2;       // A tiles per work item
 constexpr int kMaxStages = 6;   // B ring depth limit
 constexpr int kAccCols = kTiles * BN;  // one accumulator per tile slot: 512 columns
 constexpr int kBarriers = 48;          // mbarrier slots in shared memory
+// Shared memory of the per-item partials handed to the merge warp, two
+// buffers (item parity) of pass 1 [tile slot][half][128 rows][max, sum] or
+// pass 2 [tile slot][half][128 slots].
+__host__ __device__ constexpr int part_bytes(int pass) {
+  return 2 * kTiles * 2 * BM * (pass == 1 ? 8 : 4);
+}
 
 struct Params {
   int U, T, R, Rp, W, B, H;
   int n_items, n_tiles, n_pairs, n_stages, unit_major;
+  int rb_shift;  // log2 of the pass-2 row-constant buffers (2, or 1 for the largest R)
   float scale_log2;
   const int32_t* pad;
   float* negb;    // [U][Rp] -b_r (pass 1 writes, pass 2 reads by bulk copy)
@@ -110,15 +120,16 @@ __device__ __forceinline__ int chunk_cols(const Item& it, int ch) {
 // Shared-memory layout (byte offsets from the 1024-aligned base).
 struct Layout {
   int a_bytes, b_bytes;  // per tile / per stage
-  int off_b, off_bars, off_misc, off_rowb, total;
-  __host__ __device__ Layout(int D, int n_stages, int rowb_floats) {
+  int off_b, off_bars, off_misc, off_rowb, off_part, total;
+  __host__ __device__ Layout(int D, int n_stages, int rowb_bytes, int part_bytes) {
     a_bytes = BM * D * 2;
     b_bytes = BN * D * 2;
     off_b = kTiles * a_bytes;  // A: one buffer per tile slot
     off_bars = off_b + n_stages * b_bytes;
     off_misc = off_bars + kBarriers * 8;
     off_rowb = off_misc + 16;
-    total = 1024 + off_rowb + 2 * rowb_floats * 4;
+    off_part = off_rowb + rowb_bytes;
+    total = 1024 + off_part + part_bytes;
   }
 };
 
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap map_b, Params p) {
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ >= 1000)
   const int rbf = (PASS == 2) ? rowb_floats(p.R) : 0;
-  const Layout ly(D, p.n_stages, rbf);
+  const Layout ly(D, p.n_stages, (rbf * 4) << p.rb_shift, part_bytes(PASS));
   const int NS = p.n_stages;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle, as an offset from the shared
@@ -375,13 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* done = accempty + kTiles;         // [1]
   uint64_t* rbfull = done + 1;                // [2] pass 2 row constants landed
   uint64_t* rbempty = rbfull + 2;             // [2] ... consumed (all epilogue warps)
-  uint64_t* mrg_full = rbempty + 2;           // [8] half 1's partials stored (slot x quarter)
-  uint64_t* mrg_empty = mrg_full + 2 * 4;     // [8] half 0 has read them
-  static_assert(2 * kMaxStages + 4 * kTiles + 1 + 2 + 2 + 8 + 8 <= kBarriers,
+  uint64_t* part_full = rbempty + 2;          // [2][kTiles] both halves' partials stored
+  uint64_t* part_empty = part_full + 2 * kTiles;  // [2][kTiles] ... read by the merge warp
+  static_assert(2 * kMaxStages + 4 * kTiles + 1 + 2 + 2 + 4 * kTiles <= kBarriers,
                 "barrier area too small");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + ly.off_misc);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + ly.off_misc + 4);
   float* row_b_all = reinterpret_cast<float*>(smem + ly.off_rowb);
+  float* part = reinterpret_cast<float*>(smem + ly.off_part);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -399,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&rbfull[b], 1);
       mbar_init(&rbempty[b], kEpiWarps);
     }
-    for (int m = 0; m < 8; ++m) {
-      mbar_init(&mrg_full[m], 1);
-      mbar_init(&mrg_empty[m], 1);
+    for (int m = 0; m < 2 * kTiles; ++m) {
+      mbar_init(&part_full[m], 8);  // 4 lane quarters x 2 column halves
+      mbar_init(&part_empty[m], 1);
     }
     mbar_init(done, 1);
     *abort = 0;
@@ -411,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if constexpr (PASS == 2) {
     // rows past the unit's constants never get copied: they must contribute 0
-    for (int i = threadIdx.x; i < 2 * rbf; i += kThreads) {
+    for (int i = threadIdx.x; i < (rbf << p.rb_shift); i += kThreads) {
       const int r = i % rbf;
       if (r >= p.Rp) row_b_all[i] = -INFINITY;
     }
@@ -469,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(a_buf + t * ly.a_bytes, &map_a, 0, it.a_row[t], 0, &afull[t]);
         }
         if (ok && PASS == 2) {
-          const int rb = rb_iter & 1;
-          if (!mbar_wait(&rbempty[rb], ((rb_iter >> 1) & 1) ^ 1, abort, p.status)) break;
+          const int rb = rb_iter & p.rb_shift;
+          if (!mbar_wait(&rbempty[rb], ((rb_iter >> p.rb_shift) & 1) ^ 1, abort, p.status)) break;
           ++rb_iter;
           mbar_arrive_expect_tx(&rbfull[rb], p.Rp * 4);
           bulk_load(row_b_all + rb * rbf, p.negb + static_cast<size_t>(it.u) * p.Rp,
@@ -480,8 +492,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int t = 0; t < kTiles; ++t)
         if (a_cnt[t] > 0) drain_wait(&afull[t], (a_cnt[t] - 1) & 1, p.status);
-      for (int i = (rb_iter > 2 ? rb_iter - 2 : 0); i < rb_iter; ++i)
-        drain_wait(&rbfull[i & 1], (i >> 1) & 1, p.status);
+      const int n_rb = 1 << p.rb_shift;
+      for (int i = (rb_iter > n_rb ? rb_iter - n_rb : 0); i < rb_iter; ++i)
+        drain_wait(&rbfull[i & p.rb_shift], (i >> p.rb_shift) & 1, p.status);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -538,14 +551,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(done, 0, p.status);
     }
     __syncwarp();
+  } else if (warp == kMergeWarp) {
+    // ------------------------------------------------------------ merge
+    // Combines the two column halves' partials of every item and tile slot
+    // (handed over in shared memory) and writes the results, off the
+    // epilogue's path: lane i takes rows (pass 1) or slots (pass 2) i + 32j.
+    const float c = p.scale_log2;
+    int n_merge[kTiles] = {0, 0};
+    bool ok = true;
+    for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
+      const Item it = decode<PASS>(p, item);
+      if (PASS == 2 && it.n_ch == 0) continue;  // the epilogue skips these items
+#pragma unroll
+      for (int t = 0; t < kTiles; ++t) {
+        const int tile = it.tile[t];
+        if (!ok || tile < 0) continue;
+        const int pb = (n_merge[t] & 1) * kTiles + t;
+        if (!epi_wait(&part_full[pb], (n_merge[t] >> 1) & 1, abort, p.status, lane)) {
+          ok = false;
+          continue;
+        }
+        ++n_merge[t];
+        float a0[4], a1[4], b0[4], b1[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int lrow = lane + 32 * j;
+          if (PASS == 1) {
+            const float* h0 = part + (pb * 2 + 0) * BM * 2;
+            const float* h1 = part + (pb * 2 + 1) * BM * 2;
+            a0[j] = h0[2 * lrow];
+            b0[j] = h0[2 * lrow + 1];
+            a1[j] = h1[2 * lrow];
+            b1[j] = h1[2 * lrow + 1];
+          } else {
+            a0[j] = part[(pb * 2 + 0) * BM + lrow];
+            a1[j] = part[(pb * 2 + 1) * BM + lrow];
+            b0[j] = b1[j] = 0.f;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&part_empty[pb]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int lrow = lane + 32 * j;
+          if (PASS == 1) {
+            const int r = tile * BM + lrow;
+            const int qpos = p.T - p.W + (r % p.W);
+            const bool row_valid = (r < p.R) && (qpos >= it.pad) && (it.n_ch > 0);
+            if (r < p.Rp) {
+              // (max, sum) of columns [0, 128) and [128, 256) of every chunk
+              const float mz = a0[j], sum = b0[j], m2 = a1[j], s2 = b1[j];
+              const float M = fmaxf(mz, m2);
+              const float S = (M == -INFINITY)
+                                  ? 0.f
+                                  : sum * ex2((mz - M) * c) + s2 * ex2((m2 - M) * c);
+              const bool has = row_valid && S > 0.f;
+              const size_t o = static_cast<size_t>(it.u) * p.Rp + r;
+              p.negb[o] = has ? -(M * c + log2f(S)) : -INFINITY;
+              p.pmax[o] = has ? 1.0f / S : 0.f;
+            }
+          } else {
+            const int pos = tile * BM + lrow;
+            if (pos >= it.pad && pos < p.T)
+              p.usage[static_cast<size_t>(it.u) * p.T + pos] = a0[j] + a1[j];
+          }
+        }
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp 2 + 4g + i (g = 0..3): tile slot g & 1, column half g >> 1 of the
     // slot's accumulator; lane quarter warp % 4 (the TMEM lanes a warp may
     // access).  Four epilogue warps per SM sub-partition hide each other's
-    // TMEM-load and barrier latency.  The two halves of a row (pass 1) or slot
-    // (pass 2) combine at the end of the item: half 1 stores its partial where
-    // the result goes and signals, half 0 reads it back and writes the result.
+    // TMEM-load and barrier latency.  At the end of an item both halves store
+    // their partial of each row (pass 1) or slot (pass 2) in shared memory for
+    // the merge warp and go on with the next item.
     const int grp = (warp - 2) >> 2;
     const int wg = grp & 1;            // tile slot
     const int half = grp >> 1;         // accumulator columns [128 half, 128 half + 128)
@@ -553,10 +633,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lrow = quarter * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                             static_cast<uint32_t>(wg * BN + half * kHalf);
-    const int tq = wg * 4 + quarter;   // merge barrier pair of this (tile slot, quarter)
     const float c = p.scale_log2;
     int k = 0;        // accumulator fills of this tile slot consumed
-    int n_merge = 0;  // merges of this (tile slot, quarter): both halves count alike
+    int n_merge = 0;  // items of this tile slot handed to the merge warp
     int rb_iter = 0;
     bool ok = true;
     auto release = [&]() {
@@ -615,41 +694,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if (tile < 0) continue;
-        const size_t o = static_cast<size_t>(it.u) * p.Rp + r;
-        const bool in_rows = r < p.Rp;
-        if (half == 1) {
-          // partial (max, sum) of columns [128, 256) of every chunk
-          if (!epi_wait(&mrg_empty[tq], (n_merge & 1) ^ 1, abort, p.status, lane)) break;
-          if (in_rows) {
-            p.negb[o] = mz;
-            p.pmax[o] = sum;
-          }
-          __threadfence_block();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&mrg_full[tq]);
-        } else {
-          if (!epi_wait(&mrg_full[tq], n_merge & 1, abort, p.status, lane)) break;
-          __syncwarp();
-          const float m2 = in_rows ? __ldcg(p.negb + o) : -INFINITY;
-          const float s2 = in_rows ? __ldcg(p.pmax + o) : 0.f;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&mrg_empty[tq]);
-          const float M = fmaxf(mz, m2);
-          const float S = (M == -INFINITY)
-                              ? 0.f
-                              : sum * ex2((mz - M) * c) + s2 * ex2((m2 - M) * c);
-          if (in_rows) {
-            const bool has = row_valid && S > 0.f;
-            p.negb[o] = has ? -(M * c + log2f(S)) : -INFINITY;
-            p.pmax[o] = has ? 1.0f / S : 0.f;
-          }
-        }
+        // partial (max, sum) of this half's columns of every chunk
+        const int pb = (n_merge & 1) * kTiles + wg;
+        if (!epi_wait(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status, lane)) break;
+        *reinterpret_cast<float2*>(part + ((pb * 2 + half) * BM + lrow) * 2) = make_float2(mz, sum);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&part_full[pb]);
         ++n_merge;
       } else {
         if (it.n_ch == 0) continue;
         // the unit's negated row constants (bulk copy by the loader warp)
-        const int rb = rb_iter & 1;
-        if (!epi_wait(&rbfull[rb], (rb_iter >> 1) & 1, abort, p.status, lane)) break;
+        const int rb = rb_iter & p.rb_shift;
+        if (!epi_wait(&rbfull[rb], (rb_iter >> p.rb_shift) & 1, abort, p.status, lane)) break;
         ++rb_iter;
         const float* row_b = row_b_all + rb * rbf;
         const int pos = (tile >= 0 ? tile : 0) * BM + lrow;
@@ -696,23 +752,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&rbempty[rb]);
         if (!ok) break;
         if (tile < 0) continue;
-        const float part = acc.x + acc.y;
-        float* dst = p.usage + static_cast<size_t>(it.u) * p.T + pos;
-        if (half == 1) {
-          // partial usage over the query rows of columns [128, 256) of every chunk
-          if (!epi_wait(&mrg_empty[tq], (n_merge & 1) ^ 1, abort, p.status, lane)) break;
-          if (pos_valid) *dst = part;
-          __threadfence_block();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&mrg_full[tq]);
-        } else {
-          if (!epi_wait(&mrg_full[tq], n_merge & 1, abort, p.status, lane)) break;
-          __syncwarp();
-          const float other = pos_valid ? __ldcg(dst) : 0.f;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&mrg_empty[tq]);
-          if (pos_valid) *dst = part + other;
-        }
+        // partial usage over the query rows of this half's columns of every chunk
+        const int pb = (n_merge & 1) * kTiles + wg;
+        if (!epi_wait(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status, lane)) break;
+        part[(pb * 2 + half) * BM + lrow] = acc.x + acc.y;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&part_full[pb]);
         ++n_merge;
       }
     }
@@ -786,9 +831,9 @@ int smem_optin() {
 }
 
 // The deepest B ring (at least 2 stages) that fits next to the A tiles.
-int pick_stages(int D, int rbf) {
+int pick_stages(int D, int rowb_bytes, int part_bytes) {
   for (int s = kMaxStages; s >= 2; --s)
-    if (Layout(D, s, rbf).total <= smem_optin()) return s;
+    if (Layout(D, s, rowb_bytes, part_bytes).total <= smem_optin()) return s;
   return 0;
 }
 
@@ -821,12 +866,13 @@ cudaError_t launch_d(const kvc_handle* h, const UsageArgs& a, int pass, cudaStre
   p.status = h->ws.status;
 
   const int rbf = (pass == 2) ? rowb_floats(dm.R) : 0;
-  p.n_stages = pick_stages(D, rbf);
+  p.rb_shift = Layout(D, 2, 2 * rbf * 4, part_bytes(pass)).total <= smem_optin() ? 1 : 0;
+  p.n_stages = pick_stages(D, (rbf * 4) << p.rb_shift, part_bytes(pass));
   if (p.n_stages == 0) {
     if (err) *err = "attention kernel does not fit in shared memory";
     return cudaErrorInvalidValue;
   }
-  const size_t smem = Layout(D, p.n_stages, rbf).total;
+  const size_t smem = Layout(D, p.n_stages, (rbf * 4) << p.rb_shift, part_bytes(pass)).total;
   p.n_tiles = (pass == 1) ? (dm.R + BM - 1) / BM : (a.T + BM - 1) / BM;
   p.n_pairs = (p.n_tiles + kTiles - 1) / kTiles;
   p.n_items = dm.U * p.n_pairs;
@@ -862,9 +908,12 @@ cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a, int 
   }
 }
 
-// Shared memory the attention kernels need with their shallowest ring (2 stages).
+// Shared memory the attention kernels need with their shallowest ring (2 stages)
+// and a single row-constant buffer.
 size_t attention_usage_smem_bytes(int d, int R) {
-  return static_cast<size_t>(Layout(d, 2, rowb_floats(R)).total);
+  const int p1 = Layout(d, 2, 0, part_bytes(1)).total;
+  const int p2 = Layout(d, 2, rowb_floats(R) * 4, part_bytes(2)).total;
+  return static_cast<size_t>(p1 > p2 ? p1 : p2);
 }
 
 int attention_row_stride(int R) { return round4(R); }
