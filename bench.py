@@ -62,7 +62,7 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=None,
                     help="the same workload recipe cut to this many layers (small profiling case)")
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-layers", type=int, default=4,
+    ap.add_argument("--e2e-layers", type=int, default=2,
                     help="layers per host<->device copy stage of the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")

@@ -389,7 +389,7 @@ class Handle:
         return h2d, d2h
 
     def event_from_host(self, host_in: dict, dev_in: dict, host_out: dict, dev_out: dict,
-                        T: int, layers_per_stage: int = 4, stream=None):
+                        T: int, layers_per_stage: int = 2, stream=None):
         """kvc_event_host: the event from pinned host buffers, pipelined over
         groups of layers (host -> device copies of the next group and device ->
         host copies of the previous one overlap the current group's event).
