@@ -174,8 +174,11 @@ __global__ void __launch_bounds__(kThreads)
 // over its slots, then block_sum) are those of the general kernel below.
 constexpr int kSmemT = 4096;
 
+// Latency-bound: one CTA per unit, so the more CTAs an SM holds the better.
+// Up to 8 slots per thread the kernel fits in 32 registers without spilling,
+// which lets 8 CTAs share an SM (5 at its natural 47 registers).
 template <int kEpt>  // slots per thread: T <= kEpt * kThreads
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kEpt <= 8 ? 8 : 4)
     mass_post_smem_kernel(PostParams p) {
   __shared__ float red[kThreads / 32 + 1];
   __shared__ float a[kEpt * kThreads];

@@ -204,7 +204,9 @@ __device__ void take_best_bids(const int64_t* rem, const int32_t* ref, int32_t* 
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// 12 CTAs per SM (40 registers) rather than 10 at the natural 48: the kernel
+// is latency-bound per unit, and more units in flight shorten the launch.
+__global__ void __launch_bounds__(kThreads, 12)
     segment_quota_kernel(SegParams p) {
   extern __shared__ uint8_t sm[];
   // dynamic shared layout: seg mass (u64) | rem (i64) | start | len | quota |
