@@ -61,7 +61,7 @@ def parse_args():
     ap.add_argument("--workload", default="qwen_28l")
     ap.add_argument("--layers", type=int, default=None,
                     help="the same workload recipe cut to this many layers (small profiling case)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--e2e-layers", type=int, default=2,
                     help="layers per host<->device copy stage of the end-to-end leg")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -71,6 +71,9 @@ def parse_args():
                     help="compact into a paged KV pool (block size 16) instead of dense caches")
     ap.add_argument("--ablation", choices=sorted(ABLATIONS), default="none",
                     help="time one of the method's ablations (the pages' ablation table)")
+    ap.add_argument("--grouped", type=int, default=0, metavar="G",
+                    help="ragged batch sorted by length and run in groups of G sequences, each "
+                         "padded only to its own longest sequence (SkipKV's batch grouping)")
     ap.add_argument("--redundancy", type=float, default=0.0, metavar="SIGMA",
                     help="select on the SkipKV key-redundancy mix with this sigma (0.1 in the "
                          "pages); 0 = the attention score alone")
@@ -274,11 +277,13 @@ def run_reference(args, w):
     q, k, v, c, pad, nc = unit_inputs(inp)
     U = q.shape[0]
     T = k.shape[1]
+    cores = host_cores()
 
     def step(i):
-        u = i % U
-        oracle.event(p, q[u:u + 1], k[u:u + 1], v[u:u + 1], c[u:u + 1], pad[u:u + 1], nc[u:u + 1])
-        return T - int(pad[u])
+        """One step: `cores` units of the workload at once, one per host core."""
+        us = [(i * cores + j) % U for j in range(cores)]
+        oracle.event(p, q[us], k[us], v[us], c[us], pad[us], nc[us], threads=cores)
+        return sum(T - int(pad[u]) for u in us)
 
     for i in range(args.warmup):
         step(i)
@@ -288,23 +293,25 @@ def run_reference(args, w):
         tokens += step(i)
     dt = time.perf_counter() - t0
     value = tokens / dt
-    sample = (f"{args.steps} steps, each one unit (one sequence x one KV head x one layer, "
-              f"T={T}, G={w.group}, W={w.window}, d={w.head_dim}) of the {w.name} workload; "
-              f"single-threaded C oracle (fp64)")
+    sample = (f"{args.steps} steps, each {cores} units (one sequence x one KV head x one layer, "
+              f"T={T}, G={w.group}, W={w.window}, d={w.head_dim}) of the {w.name} workload, "
+              f"one unit per host core; C oracle (fp64) through a thread pool")
+    world = dist_env()[0]
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": workload_config(w, T, args.ablation, redundancy=args.redundancy),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "config": dict(workload_config(w, T, args.ablation, redundancy=args.redundancy),
+                       parallelism=f"replicas x{world}"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
 
-def workload_config(w, T, ablation="none", paged=False, redundancy=0.0):
+def workload_config(w, T, ablation="none", paged=False, redundancy=0.0, grouped=0):
     cfg = {"workload": (f"{w.name}: {w.n_layers} layers x batch {w.batch} x {w.n_kv_heads} KV heads"
                          f" (GQA {w.group}), d {w.head_dim}, {T} slots -> budget {w.budget}, "
                          f"window {w.window}" + (", event 2 (credit carried, 512 fresh slots)"
@@ -319,10 +326,100 @@ def workload_config(w, T, ablation="none", paged=False, redundancy=0.0):
                         "sigma * score/sum(score) - (1 - sigma) * softmax(mean key cosine)")
     if paged:
         cfg["paged"] = "compaction into a paged pool, block size 16 (stack and table restored per step)"
+    if grouped:
+        cfg["layout"] = (f"sequences sorted by length, {w.batch // grouped} events of {grouped} "
+                         "sequences, each padded to its own longest sequence")
+    elif w.prefill is not None:
+        cfg["layout"] = f"left-padded to the longest sequence ({T} slots)"
     return cfg
 
 
 # ------------------------------------------------------------------ our arm
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_oracle_baseline(args, w, parts):
+    """The oracle as it stands, on a bounded random sample of the timed event's
+    units: single-threaded for about half of --cpu-seconds, then the units split
+    over a thread pool on every host core for about the other half (units are
+    independent; ctypes releases the GIL in the C calls).  Unit data are copied
+    to the host before each timed part."""
+    import numpy as np
+
+    import oracle
+    import workload as wl
+    oracle.build()
+    p = oracle.RefParams(group=w.group, head_dim=w.head_dim, window=w.window, budget=w.budget,
+                         n_sink=w.n_sink, n_recent=w.n_recent, **method_kw(args))
+    pool = [(j, u) for j, part in enumerate(parts) for u in range(part["w"].units)]
+    order = np.random.default_rng(0).permutation(len(pool))
+    nxt = 0
+
+    def take(n):
+        """Host copies of the next n sampled units: (inputs, valid tokens)."""
+        nonlocal nxt
+        chosen = [pool[i] for i in order[nxt:nxt + n]]
+        nxt += len(chosen)
+        cols = [[] for _ in range(6)]
+        tokens = 0
+        for j, u in chosen:
+            inp, pw = parts[j]["inp"], parts[j]["w"]
+            sl = slice(u, u + 1)
+            pad_u = wl.unit_pad(inp)[sl]
+            vals = (wl.bf16_bits(wl.q_units(inp.q, pw)[sl]), wl.bf16_bits(wl.units_of(inp.k, pw)[sl]),
+                    wl.bf16_bits(wl.units_of(inp.v, pw)[sl]),
+                    wl.units_of(inp.credit, pw)[sl].cpu().numpy(), pad_u.cpu().numpy(),
+                    wl.unit_n_carry(inp)[sl].cpu().numpy())
+            for c, v in zip(cols, vals):
+                c.append(v)
+            tokens += parts[j]["T"] - int(pad_u.item())
+        return cols, tokens
+
+    def run(cols, threads):
+        # units of different groups differ in T: one call per unit in that case
+        if len({c.shape[1] for c in cols[1]}) == 1:
+            arrs = [np.concatenate(c, axis=0) for c in cols]
+            t0 = time.perf_counter()
+            oracle.event(p, *arrs, threads=threads)
+            return time.perf_counter() - t0
+        from concurrent.futures import ThreadPoolExecutor
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(lambda i: oracle.event(p, *[c[i] for c in cols]), range(len(cols[0]))))
+        return time.perf_counter() - t0
+
+    half = args.cpu_seconds / 2
+    done1 = tok1 = 0
+    dt1 = 0.0
+    while nxt < len(pool) and (dt1 < half or done1 == 0):
+        cols, tokens = take(1)
+        dt1 += run(cols, 1)
+        done1 += 1
+        tok1 += tokens
+    rate1 = tok1 / dt1
+    cores = host_cores()
+    per_unit = dt1 / done1
+    n_all = int(min(len(pool) - nxt, max(cores, cores * half / per_unit)))
+    n_all = max(1, n_all - n_all % cores if n_all >= cores else n_all)
+    value, used, sample_all = rate1, 1, None
+    if n_all > 0 and nxt < len(pool):
+        cols, tokens = take(n_all)
+        used = min(cores, n_all)
+        dtn = run(cols, used)
+        value = tokens / dtn
+        sample_all = f"{n_all} further units on {used} threads ({dtn:.1f} s)"
+    return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
+            "single_core_value": rate1,
+            "sample": (f"random units of the timed event (seed 0), same inputs, C oracle in fp64: "
+                       f"{done1} units single-threaded ({dt1:.1f} s, value {rate1:.4g} tokens/s)"
+                       + (f"; {sample_all} give the value, cores = threads used"
+                          if sample_all else "; value = single-threaded"))}
+
 
 def run_ours(args, w):
     import numpy as np
@@ -357,13 +454,43 @@ def run_ours(args, w):
         del o1, first
         torch.cuda.empty_cache()
     T = inp.T
-    out = h.outputs(T, dev)
     stream = torch.cuda.current_stream(dev)
-    tokens_per_step = float(w.n_layers * w.n_kv_heads * (T - inp.pad.long()).sum().item())
+    # the timed work: one event per part (one part, or the length-sorted groups)
+    if args.grouped:
+        assert w.prefill is not None and w.n_events == 1, "--grouped needs a ragged workload"
+        assert w.batch % args.grouped == 0, "the batch must split into equal groups"
+        lengths = (T - inp.pad.long()).cpu().numpy()
+        by_len = np.argsort(lengths, kind="stable")
+        gw = wl.scaled(w, batch=args.grouped)
+        h.close()
+        h = kvc.Handle(kvc.Config(w.n_layers, args.grouped, w.n_kv_heads, w.group, w.head_dim,
+                                  T, w.budget, window=w.window, n_sink=w.n_sink,
+                                  n_recent=w.n_recent, **method_kw(args)))
+        parts = []
+        for g0 in range(0, w.batch, args.grouped):
+            grp = by_len[g0:g0 + args.grouped]
+            Tg = int(lengths[grp].max())
+            idx = torch.as_tensor(grp, device=dev, dtype=torch.long)
+            pad_g = torch.as_tensor(Tg - lengths[grp], device=dev).to(torch.int32)
+            gi = wl.Inputs(gw, Tg, inp.q.index_select(1, idx).contiguous(),
+                           inp.k.index_select(1, idx)[:, :, :, T - Tg:].contiguous(),
+                           inp.v.index_select(1, idx)[:, :, :, T - Tg:].contiguous(),
+                           inp.credit.index_select(1, idx)[:, :, :, T - Tg:].contiguous(),
+                           pad_g, (Tg - pad_g).to(torch.int32))
+            parts.append({"inp": gi, "T": Tg, "w": gw, "out": h.outputs(Tg, dev)})
+        del inp
+        torch.cuda.empty_cache()
+    else:
+        parts = [{"inp": inp, "T": T, "w": w, "out": h.outputs(T, dev)}]
+    inp, out = parts[0]["inp"], parts[0]["out"]
+    tokens_per_step = float(sum(pt["w"].n_layers * pt["w"].n_kv_heads
+                                * (pt["T"] - pt["inp"].pad.long()).sum().item() for pt in parts))
 
     def step():
-        h.event(inp.q, inp.k, inp.v, T, inp.pad, inp.n_carry, inp.credit, out["k_out"],
-                out["v_out"], out["credit_out"], out["kept_idx"], out["n_kept"])
+        for pt in parts:
+            x, o = pt["inp"], pt["out"]
+            h.event(x.q, x.k, x.v, pt["T"], x.pad, x.n_carry, x.credit, o["k_out"],
+                    o["v_out"], o["credit_out"], o["kept_idx"], o["n_kept"])
 
     if args.paged:
         args.no_e2e = True  # the host round trip is timed for the dense path only
@@ -458,18 +585,18 @@ def run_ours(args, w):
 
     # ---- roofline of the dominant kernel and of the event
     peaks, peak_src = load_peaks()
-    lengths = (T - inp.pad.long()).cpu().numpy()
     flops_ev = bytes_ev = 0.0
     per_kernel_work = {}
-    for Tv in lengths:
-        f, b, pk = unit_work(w, int(Tv), T)
-        n_u = w.n_layers * w.n_kv_heads
-        flops_ev += f * n_u
-        bytes_ev += b * n_u
-        for name, (bound, fl, by) in pk.items():
-            acc = per_kernel_work.setdefault(name, [bound, 0.0, 0.0])
-            acc[1] += fl * n_u
-            acc[2] += by * n_u
+    for pt in parts:
+        for Tv in (pt["T"] - pt["inp"].pad.long()).cpu().numpy():
+            f, b, pk = unit_work(w, int(Tv), pt["T"])
+            n_u = w.n_layers * w.n_kv_heads
+            flops_ev += f * n_u
+            bytes_ev += b * n_u
+            for name, (bound, fl, by) in pk.items():
+                acc = per_kernel_work.setdefault(name, [bound, 0.0, 0.0])
+                acc[1] += fl * n_u / len(parts)   # per launch: each part is one launch
+                acc[2] += by * n_u / len(parts)
     total_kernel_ms = sum(k["total_ms"] for k in kernels) or 1.0
     krows = []
     for k in kernels:
@@ -503,24 +630,38 @@ def run_ours(args, w):
     # ---- end to end through host buffers
     e2e = None
     if not args.no_e2e:
-        host_in = {k: getattr(inp, k).cpu().pin_memory() for k in
-                   ("q", "k", "v", "credit", "pad", "n_carry")}
-        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-                    for k, v in out.items()}
-        dev_in = {k: getattr(inp, k) for k in ("q", "k", "v", "credit", "pad", "n_carry")}
-        dev_in = {k: torch.empty_like(v) for k, v in dev_in.items()}  # staging, as a caller has
         lps = args.e2e_layers
-        h.event_from_host(host_in, dev_in, host_out, out, T, layers_per_stage=lps)  # warm-up
+        legs = []
+        for pt in parts:
+            x = pt["inp"]
+            host_in = {k: getattr(x, k).cpu().pin_memory() for k in
+                       ("q", "k", "v", "credit", "pad", "n_carry")}
+            host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                        for k, v in pt["out"].items()}
+            dev_in = {k: torch.empty_like(getattr(x, k))  # staging, as a caller has
+                      for k in ("q", "k", "v", "credit", "pad", "n_carry")}
+            legs.append((host_in, dev_in, host_out, pt))
+
+        def e2e_step():
+            h2d_s = d2h_s = 0
+            for host_in, dev_in, host_out, pt in legs:
+                a, b = h.event_from_host(host_in, dev_in, host_out, pt["out"], pt["T"],
+                                         layers_per_stage=lps)
+                h2d_s += a
+                d2h_s += b
+            return h2d_s, d2h_s
+
+        e2e_step()  # warm-up
         torch.cuda.synchronize(dev)
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(stream)
         for _ in range(args.e2e_steps):
-            h2d, d2h = h.event_from_host(host_in, dev_in, host_out, out, T, layers_per_stage=lps)
+            h2d, d2h = e2e_step()
         f1.record(stream)
         torch.cuda.synchronize(dev)
         # V is read in place at the kept rows (page-locked host buffer)
-        h2d += int(host_out["n_kept"].long().sum().item()) * w.head_dim * 2
+        h2d += sum(int(leg[2]["n_kept"].long().sum().item()) for leg in legs) * w.head_dim * 2
         e2e_ms = f0.elapsed_time(f1) / args.e2e_steps
         e2e_ms, _ = reduce_over_ranks(e2e_ms, 0.0, dev)
         e2e = {"value": total_tokens / (e2e_ms / 1000.0), "unit": UNIT,
@@ -528,38 +669,12 @@ def run_ours(args, w):
                "steps": args.e2e_steps,
                "path": f"kvc_event_host, pinned host buffers, {lps} layers per copy stage; "
                        "V read in place at the kept rows"}
-        del host_in, host_out
+        del legs
 
     # ---- CPU oracle baseline on a bounded sample (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-        oracle.build()
-        p = oracle.RefParams(group=w.group, head_dim=w.head_dim, window=w.window,
-                             budget=w.budget, n_sink=w.n_sink, n_recent=w.n_recent,
-                             **method_kw(args))
-        q_u = wl.q_units(inp.q, w)
-        k_u = wl.units_of(inp.k, w)
-        v_u = wl.units_of(inp.v, w)
-        c_u = wl.units_of(inp.credit, w)
-        pad_u = wl.unit_pad(inp)
-        nc_u = wl.unit_n_carry(inp)
-        rng = np.random.default_rng(0)
-        order = rng.permutation(w.units)
-        t0 = time.perf_counter()
-        done = tokens = 0
-        while done < len(order) and (time.perf_counter() - t0 < args.cpu_seconds or done == 0):
-            u = int(order[done])
-            oracle.event(p, wl.bf16_bits(q_u[u:u + 1]), wl.bf16_bits(k_u[u:u + 1]),
-                         wl.bf16_bits(v_u[u:u + 1]), c_u[u:u + 1].cpu().numpy(),
-                         pad_u[u:u + 1].cpu().numpy(), nc_u[u:u + 1].cpu().numpy())
-            tokens += T - int(pad_u[u])
-            done += 1
-        dt = time.perf_counter() - t0
-        cpu = {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{done} of {w.units} units of the timed event (random, seed 0), "
-                         f"same inputs, single-threaded C oracle (fp64); host copies included"}
-
+        cpu = cpu_oracle_baseline(args, w, parts)
     clocks = summarize_clocks(clock_rows, t_wall0, t_wall1)
     # kernels per traced entry (the paged compaction is four launches)
     launches = sum(r["launches"] * (4 if r["name"] == "compact_paged" else 1) for r in krows)
@@ -567,7 +682,8 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": warm, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w, T, args.ablation, args.paged, args.redundancy),
+        "config": dict(workload_config(w, T, args.ablation, args.paged, args.redundancy,
+                                       args.grouped),
                        parallelism=f"replicas x{world}"),
         "roofline": roofline, "event_roofline": event_roofline,
         "kernels": [{k2: (round(v, 6) if isinstance(v, float) else v) for k2, v in r.items()}

@@ -17,8 +17,12 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRowsPerBlock = 128;
 
+// gridDim.y is at most 65535: larger unit counts launch in chunks of units
+constexpr int kMaxGridY = 65535;
+
 struct CompactParams {
   int T, budget, vecs;  // vecs = 16-byte vectors per row
+  int unit0;            // first unit of this launch
   const uint4* k;
   const uint4* v;
   const float* credit;
@@ -33,7 +37,7 @@ struct CompactParams {
 __global__ void __launch_bounds__(kThreads)
     compact_kernel(CompactParams p) {
   __shared__ int32_t s_src[kRowsPerBlock];
-  const int u = blockIdx.y;
+  const int u = p.unit0 + static_cast<int>(blockIdx.y);
   const int r0 = blockIdx.x * kRowsPerBlock;
   const int rows = min(kRowsPerBlock, p.budget - r0);
   const int nk = p.n_kept[u];
@@ -101,8 +105,12 @@ cudaError_t launch_compact(const kvc_handle* h, const uint16_t* k,
   p.v_out = reinterpret_cast<uint4*>(v_out);
   p.credit_out = credit_out;
   p.status = h->ws.status;
-  dim3 grid((p.budget + kRowsPerBlock - 1) / kRowsPerBlock, h->dims.U);
-  compact_kernel<<<grid, kThreads, 0, s>>>(p);
+  const int U = h->dims.U;
+  for (int u0 = 0; u0 < U; u0 += kMaxGridY) {
+    p.unit0 = u0;
+    dim3 grid((p.budget + kRowsPerBlock - 1) / kRowsPerBlock, min(kMaxGridY, U - u0));
+    compact_kernel<<<grid, kThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

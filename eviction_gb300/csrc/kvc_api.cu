@@ -30,54 +30,6 @@ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
-int validate_config(const kvc_config* c, std::string* why) {
-  auto bad = [&](const char* m) {
-    *why = m;
-    return KVC_ERR_ARG;
-  };
-  if (!c) return bad("config is null");
-  if (c->n_layers < 1 || c->batch < 1 || c->n_kv_heads < 1 || c->group < 1)
-    return bad("n_layers, batch, n_kv_heads and group must be >= 1");
-  if (c->window < 1 || c->budget < 1 || c->max_T < 1)
-    return bad("window, budget and max_T must be >= 1");
-  if (c->max_T > kMaxT) return bad("max_T must be <= 65536");
-  if (c->avg_pool < 1 || c->avg_pool % 2 == 0 || c->max_pool < 1 || c->max_pool % 2 == 0)
-    return bad("avg_pool and max_pool must be odd and >= 1");
-  if (!std::isfinite(c->delta) || static_cast<double>(c->delta) < 1.0 / 1024.0)
-    return bad("delta must be finite and >= 1/1024");
-  if (c->seg_min < 1 || c->seg_max < 2 * c->seg_min || c->seg_max < 16 || c->seg_max > 4096)
-    return bad("need 1 <= seg_min, 2*seg_min <= seg_max, 16 <= seg_max <= 4096");
-  if (c->q_min < 0 || c->n_sink < 0 || c->n_recent < 0)
-    return bad("q_min, n_sink and n_recent must be >= 0");
-  if (!(c->lambda >= 0.f && c->lambda <= 1.f) || !(c->beta >= 0.f && c->beta <= 1.f))
-    return bad("lambda and beta must lie in [0, 1]");
-  if (!(c->eps > 0.f) || !std::isfinite(c->eps)) return bad("eps must be finite and > 0");
-  if (!(c->softmax_scale >= 0.f) || !std::isfinite(c->softmax_scale))
-    return bad("softmax_scale must be finite and >= 0");
-  if (c->seg_fixed < 0 || (c->seg_fixed > 0 && c->seg_fixed < c->seg_min))
-    return bad("seg_fixed must be 0 or >= seg_min");
-  if ((c->quota_by_len != 0 && c->quota_by_len != 1) ||
-      (c->global_topk != 0 && c->global_topk != 1))
-    return bad("quota_by_len and global_topk must be 0 or 1");
-  if (!(c->redundancy_sigma >= 0.f && c->redundancy_sigma <= 1.f))
-    return bad("redundancy_sigma must lie in [0, 1] (0 = off)");
-  if (c->head_dim != 64 && c->head_dim != 128) {
-    *why = "head_dim must be 64 or 128";
-    return KVC_ERR_UNSUPPORTED;
-  }
-  const long long rows = static_cast<long long>(c->group) * c->window;
-  if (rows > kMaxRows) {
-    *why = "group * window must be <= 4096";
-    return KVC_ERR_UNSUPPORTED;
-  }
-  const long long units = static_cast<long long>(c->n_layers) * c->batch * c->n_kv_heads;
-  if (units * c->max_T >= (1ll << 31) || units * rows >= (1ll << 31)) {
-    *why = "units * max_T and units * group * window must be < 2^31";
-    return KVC_ERR_UNSUPPORTED;
-  }
-  return KVC_OK;
-}
-
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
 int check_T(kvc_handle* h, int T) {
@@ -264,6 +216,58 @@ bool create_host_io(kvc::HostIO& io) {
 
 }  // namespace
 
+namespace kvc {
+
+int validate_config(const kvc_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return KVC_ERR_ARG;
+  };
+  if (!c) return bad("config is null");
+  if (c->n_layers < 1 || c->batch < 1 || c->n_kv_heads < 1 || c->group < 1)
+    return bad("n_layers, batch, n_kv_heads and group must be >= 1");
+  if (c->window < 1 || c->budget < 1 || c->max_T < 1)
+    return bad("window, budget and max_T must be >= 1");
+  if (c->max_T > kMaxT) return bad("max_T must be <= 65536");
+  if (c->avg_pool < 1 || c->avg_pool % 2 == 0 || c->max_pool < 1 || c->max_pool % 2 == 0)
+    return bad("avg_pool and max_pool must be odd and >= 1");
+  if (!std::isfinite(c->delta) || static_cast<double>(c->delta) < 1.0 / 1024.0)
+    return bad("delta must be finite and >= 1/1024");
+  if (c->seg_min < 1 || c->seg_max < 2 * c->seg_min || c->seg_max < 16 || c->seg_max > 4096)
+    return bad("need 1 <= seg_min, 2*seg_min <= seg_max, 16 <= seg_max <= 4096");
+  if (c->q_min < 0 || c->n_sink < 0 || c->n_recent < 0)
+    return bad("q_min, n_sink and n_recent must be >= 0");
+  if (!(c->lambda >= 0.f && c->lambda <= 1.f) || !(c->beta >= 0.f && c->beta <= 1.f))
+    return bad("lambda and beta must lie in [0, 1]");
+  if (!(c->eps > 0.f) || !std::isfinite(c->eps)) return bad("eps must be finite and > 0");
+  if (!(c->softmax_scale >= 0.f) || !std::isfinite(c->softmax_scale))
+    return bad("softmax_scale must be finite and >= 0");
+  if (c->seg_fixed < 0 || (c->seg_fixed > 0 && c->seg_fixed < c->seg_min))
+    return bad("seg_fixed must be 0 or >= seg_min");
+  if ((c->quota_by_len != 0 && c->quota_by_len != 1) ||
+      (c->global_topk != 0 && c->global_topk != 1))
+    return bad("quota_by_len and global_topk must be 0 or 1");
+  if (!(c->redundancy_sigma >= 0.f && c->redundancy_sigma <= 1.f))
+    return bad("redundancy_sigma must lie in [0, 1] (0 = off)");
+  if (c->head_dim != 64 && c->head_dim != 128) {
+    *why = "head_dim must be 64 or 128";
+    return KVC_ERR_UNSUPPORTED;
+  }
+  const long long rows = static_cast<long long>(c->group) * c->window;
+  if (rows > kMaxRows) {
+    *why = "group * window must be <= 4096";
+    return KVC_ERR_UNSUPPORTED;
+  }
+  const long long units = static_cast<long long>(c->n_layers) * c->batch * c->n_kv_heads;
+  if (units * c->max_T >= (1ll << 31) || units * rows >= (1ll << 31)) {
+    *why = "units * max_T and units * group * window must be < 2^31";
+    return KVC_ERR_UNSUPPORTED;
+  }
+  return KVC_OK;
+}
+
+}  // namespace kvc
+
 extern "C" {
 
 void kvc_default_config(kvc_config* c) {
@@ -307,7 +311,7 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
   if (!out) return KVC_ERR_ARG;
   *out = nullptr;
   std::string why;
-  int rc = validate_config(cfg, &why);
+  int rc = kvc::validate_config(cfg, &why);
   if (rc != KVC_OK) {
     std::fprintf(stderr, "kvc_create: %s\n", why.c_str());
     return rc;

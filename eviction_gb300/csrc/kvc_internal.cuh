@@ -126,6 +126,10 @@ cudaError_t launch_select(const kvc_handle* h, const float* score, int T,
                           const int32_t* n_seg, int32_t* kept_idx,
                           int32_t* n_kept, cudaStream_t s);
 
+// Host validation of a configuration (every field, and the unit and row counts
+// in 64-bit arithmetic); KVC_OK or a negative code with the reason in *why.
+int validate_config(const kvc_config* c, std::string* why);
+
 cudaError_t launch_compact(const kvc_handle* h, const uint16_t* k,
                            const uint16_t* v, const float* credit_post, int T,
                            const int32_t* kept_idx, const int32_t* n_kept,

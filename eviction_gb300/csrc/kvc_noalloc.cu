@@ -9,13 +9,19 @@
 // process exits.  The caller passes every input and output.
 //
 // Set-up: the first call on a device (with that device current) looks up the
-// array's device address with cudaGetSymbolAddress and caches it; make that
-// first call before any stream capture.  All calls share the array, so calls
-// that overlap on the GPU (two streams, two threads) race and must not be
-// issued; the array keeps the last call's contents, and nothing in it needs
-// to start at zero except the status word, which each call clears.
+// array's device address with cudaGetSymbolAddress and caches it (one atomic
+// slot per device, so two host threads making their first call at once both
+// store the same address); make that first call before any stream capture.  The
+// cached address belongs to the device's primary context: after
+// cudaDeviceReset on that device it is stale, and this entry point must not be
+// used on that device again in the process.  All calls share the array, so
+// calls that overlap on the GPU (two streams, two threads) race and must not be
+// issued; the array keeps the last call's contents, and nothing in it needs to
+// start at zero (every scratch value is written before it is read).
+#include <atomic>
 #include <cmath>
 #include <cstdio>
+#include <string>
 
 #include "kvc_internal.cuh"
 
@@ -30,7 +36,7 @@ namespace {
 static __device__ __align__(256) float g_noalloc_scratch[KVC_NOALLOC_SCRATCH_FLOATS];
 
 constexpr int kMaxDevices = 64;
-float* g_scratch_ptr[kMaxDevices] = {};
+std::atomic<float*> g_scratch_ptr[kMaxDevices] = {};
 
 size_t align_floats(size_t n) { return (n + 63) & ~size_t(63); }  // 256-byte steps
 
@@ -47,26 +53,24 @@ extern "C" int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const 
                                 int T, const int32_t* pad, const int32_t* n_carry,
                                 const float* credit_in, float* credit_post, float* mass,
                                 float* score, uint32_t* status, void* stream) {
-  if (!cfg) return config_error("config is null");
-  if (cfg->n_layers < 1 || cfg->batch < 1 || cfg->n_kv_heads < 1 || cfg->group < 1 ||
-      cfg->window < 1 || cfg->budget < 1 || cfg->max_T < 1 || cfg->avg_pool < 1 ||
-      cfg->avg_pool % 2 == 0 || cfg->max_pool < 1 || cfg->max_pool % 2 == 0 ||
-      !(cfg->eps > 0.f) || !(cfg->lambda >= 0.f && cfg->lambda <= 1.f) ||
-      !(cfg->beta >= 0.f && cfg->beta <= 1.f) || !(cfg->softmax_scale >= 0.f))
-    return config_error("invalid configuration value");
-  if (cfg->head_dim != 64 && cfg->head_dim != 128) {
-    std::fprintf(stderr, "kvc_mass_noalloc: head_dim must be 64 or 128\n");
-    return KVC_ERR_UNSUPPORTED;
+  std::string why;
+  const int vrc = kvc::validate_config(cfg, &why);
+  if (vrc != KVC_OK) {
+    std::fprintf(stderr, "kvc_mass_noalloc: %s\n", why.c_str());
+    return vrc;
   }
-  if (T < 1 || T > cfg->max_T || cfg->max_T > 65536) {
-    std::fprintf(stderr, "kvc_mass_noalloc: T must lie in [1, max_T], max_T <= 65536\n");
+  if (T < 1 || T > cfg->max_T) {
+    std::fprintf(stderr, "kvc_mass_noalloc: T must lie in [1, max_T]\n");
     return KVC_ERR_SHAPE;
   }
+  if (!status)
+    return config_error("status is null: device failure reports (a bounded wait that ran "
+                        "out, a bad index) have nowhere else to go");
   if (!q || !k || !pad || !n_carry || !credit_in || !credit_post || !mass || !score)
     return config_error("null pointer argument");
   if (!aligned16(q) || !aligned16(k) || !aligned16(pad) || !aligned16(n_carry) ||
       !aligned16(credit_in) || !aligned16(credit_post) || !aligned16(mass) ||
-      !aligned16(score) || (status && (reinterpret_cast<uintptr_t>(status) & 3u))) {
+      !aligned16(score) || (reinterpret_cast<uintptr_t>(status) & 3u)) {
     std::fprintf(stderr, "kvc_mass_noalloc: pointer not 16-byte aligned\n");
     return KVC_ERR_ALIGN;
   }
@@ -85,16 +89,16 @@ extern "C" int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const 
     return KVC_ERR_DEVICE;
   }
   if (major != 10 || minor != 3) return KVC_ERR_DEVICE;
-  if (!g_scratch_ptr[dev]) {
-    float* ptr = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_scratch);
-    if (e != cudaSuccess || !ptr) {
+  float* base = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (!base) {
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&base), g_noalloc_scratch);
+    if (e != cudaSuccess || !base) {
       std::fprintf(stderr, "kvc_mass_noalloc: cudaGetSymbolAddress failed: %s\n",
                    cudaGetErrorString(e));
       cudaGetLastError();
       return KVC_ERR_CUDA;
     }
-    g_scratch_ptr[dev] = ptr;
+    g_scratch_ptr[dev].store(base, std::memory_order_release);
   }
 
   // a handle on the stack: same kernels and launch shapes as kvc_mass
@@ -109,12 +113,8 @@ extern "C" int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const 
   d.G = cfg->group;
   d.W = cfg->window;
   d.d = cfg->head_dim;
-  d.R = d.G * d.W;
+  d.R = d.G * d.W;  // both products bounded by the validation above
   d.U = d.L * d.B * d.H;
-  if (d.R > 4096) {
-    std::fprintf(stderr, "kvc_mass_noalloc: group * window must be <= 4096\n");
-    return KVC_ERR_UNSUPPORTED;
-  }
   int smem_optin = 0;
   cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (kvc::attention_usage_smem_bytes(d.d, d.R) > static_cast<size_t>(smem_optin))
@@ -123,7 +123,7 @@ extern "C" int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const 
   const size_t U = d.U, Rp = kvc::attention_row_stride(d.R);
   const size_t n_negb = align_floats(U * Rp), n_pmax = align_floats(U * Rp);
   const size_t n_use = align_floats(U * static_cast<size_t>(T));
-  const size_t need = n_negb + n_pmax + n_use + 64;  // + status word
+  const size_t need = n_negb + n_pmax + n_use;
   if (need > KVC_NOALLOC_SCRATCH_FLOATS) {
     std::fprintf(stderr,
                  "kvc_mass_noalloc: needs %zu scratch floats (units * (2*rows + T)), the "
@@ -131,20 +131,13 @@ extern "C" int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const 
                  need, KVC_NOALLOC_SCRATCH_FLOATS);
     return KVC_ERR_SHAPE;
   }
-  float* base = g_scratch_ptr[dev];
   h.ws.negb = base;
   h.ws.pmax = base + n_negb;
   h.ws.usage = base + n_negb + n_pmax;
-  uint32_t* scratch_status = reinterpret_cast<uint32_t*>(base + n_negb + n_pmax + n_use);
-  h.ws.status = status ? status : scratch_status;
+  h.ws.status = status;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (!status) e = cudaMemsetAsync(scratch_status, 0, sizeof(uint32_t), s);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return KVC_ERR_CUDA;
-  }
   const double sc = cfg->softmax_scale > 0.f ? static_cast<double>(cfg->softmax_scale)
                                              : 1.0 / std::sqrt(static_cast<double>(d.d));
   kvc::UsageArgs a{q, k, pad, T, static_cast<float>(sc * 1.4426950408889634)};

@@ -29,6 +29,7 @@ constexpr int kScanThreads = 1024;
 
 struct PagedParams {
   int L, B, H, d, bs, n_blocks, max_blocks, budget, T;
+  int unit0;  // first unit of a copy launch (units go in chunks of gridDim.y <= 65535)
   uint16_t* k_pool;
   uint16_t* v_pool;
   const int32_t* seq_len;
@@ -158,7 +159,7 @@ constexpr int kCopyUnroll = 4;     // 16-byte loads in flight per thread
 __global__ void __launch_bounds__(kCopyThreads) paged_copy_kernel(PagedParams p, int vpr_log2) {
   __shared__ long long s_src[kCopyRows], s_dst[kCopyRows];  // 16-byte units; -1 = no row
   if (*p.err) return;  // the same value for every thread: written by the validation launch
-  const int u = blockIdx.y;
+  const int u = p.unit0 + static_cast<int>(blockIdx.y);
   const int h = u % p.H;
   const int b = (u / p.H) % p.B;
   const int l = u / (p.H * p.B);
@@ -273,8 +274,11 @@ cudaError_t launch_compact_paged(const kvc_handle* h, const PagedArgs& a, cudaSt
   if (e != cudaSuccess) return e;
   paged_validate_kernel<<<U, 128, 0, s>>>(p);
   paged_alloc_kernel<<<1, kScanThreads, 0, s>>>(p);
-  dim3 grid((p.budget + kCopyRows - 1) / kCopyRows, U);
-  paged_copy_kernel<<<grid, kCopyThreads, 0, s>>>(p, p.d == 64 ? 3 : 4);  // d / 8 vectors per row
+  for (int u0 = 0; u0 < U; u0 += 65535) {  // gridDim.y is at most 65535
+    p.unit0 = u0;
+    dim3 grid((p.budget + kCopyRows - 1) / kCopyRows, min(65535, U - u0));
+    paged_copy_kernel<<<grid, kCopyThreads, 0, s>>>(p, p.d == 64 ? 3 : 4);  // d / 8 vectors per row
+  }
   paged_free_kernel<<<1, kScanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }

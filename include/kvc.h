@@ -143,28 +143,66 @@ void kvc_destroy(kvc_handle* h);
 /* *s_max = max(1, T / seg_min): the segment-array stride for this T. */
 int kvc_stage_sizes(const kvc_handle* h, int T, int* s_max);
 
-/* Steps 1-2: attention usage, score, mass, credit.  Uses the handle's
- * workspace for per-query softmax statistics and the raw usage.
- * credit_in is read, credit_post written (they may be the same buffer). */
+/* Steps 1-2: attention usage, score, mass, credit.
+ * Defined by AMS, Method, Key design 1 (usage of each slot by the W most
+ * recent queries with the window-maximum fill; the 1-D average pool; the mass
+ * equation m = (max(u,0)+eps)/sum; the EMA credit c <- lambda c + (1-lambda) m
+ * and the mix m_used = normalize(beta m + (1-beta) normalize(c))), and by
+ * RefreshKV, A2 and A6 (the score: usage max-pooled over 7 neighbours).
+ *   mass, score, credit_post  [L][B][H][T] fp32 out; padding gets mass 0,
+ *   score -inf, credit 0.  Slots at or after pad+n_carry start their credit at
+ *   their current mass (the credit convention of this library).
+ * Uses the handle's workspace for per-query softmax statistics and the raw
+ * usage.  credit_in is read, credit_post written (they may be the same buffer).
+ * Host-detectable errors (null or unaligned pointer, T outside [1, max_T])
+ * return a negative code and launch nothing; a bounded wait that runs out sets
+ * KVC_STATUS_WAIT_TIMEOUT in the status word. */
 int kvc_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T,
              const int32_t* pad, const int32_t* n_carry,
              const float* credit_in, float* credit_post, float* mass,
              float* score, void* stream);
 
-/* Steps 3-4: segmentation and quotas on the fp32 mass.  Bit-exact integer
- * arithmetic (40-bit fixed-point mass, exact rational comparisons). */
+/* Steps 3-4: segmentation and quotas on the fp32 mass.
+ * Defined by AMS, Method, Key design 2 (cumulative mass C(t), cut points
+ * b_k = min{t : C(t) >= k Delta}, short segments merged and long ones split)
+ * and Key design 3 (quota = q_min + the mass-proportional share of the rest of
+ * the budget, clipped to the segment and corrected to the exact budget).
+ * Bit-exact integer arithmetic (40-bit fixed-point mass, exact rational
+ * comparisons).
+ *   mass       [L][B][H][T] fp32 (kvc_mass's m_used);
+ *   seg_start, seg_len, quota  [L][B][H][S_max] int32 out, S_max from
+ *              kvc_stage_sizes; seg_start is an absolute slot; entries past
+ *              n_seg are zero;
+ *   n_seg      [L][B][H] int32 out (0 for an all-padding sequence).
+ * A cache no longer than the budget gets quota = length everywhere. */
 int kvc_segment_quota(kvc_handle* h, const float* mass, int T,
                       const int32_t* pad, int32_t* seg_start,
                       int32_t* seg_len, int32_t* quota, int32_t* n_seg,
                       void* stream);
 
-/* Step 5 (and the index sort of step 6): kept slots per unit. */
+/* Step 5 (and the index sort of step 6): kept slots per unit.
+ * Defined by AMS, Method, Key design 3 (must-keep: the first n_sink valid
+ * slots and the last n_recent, counted inside their own segment's quota; the
+ * worked example of section "A complete example") and Key design 4 (each
+ * segment keeps its best non-must-keep slots by score, up to its quota; the
+ * union with must-keep, over-budget removal of the globally worst picks, kept
+ * slots sorted ascending).
+ *   score      [L][B][H][T] fp32 (ties go to the lower slot);
+ *   seg_*      as kvc_segment_quota writes them;
+ *   kept_idx   [L][B][H][budget] int32 out, ascending, -1 past n_kept;
+ *   n_kept     [L][B][H] int32 out = min(budget, valid slots). */
 int kvc_select(kvc_handle* h, const float* score, int T, const int32_t* pad,
                const int32_t* seg_start, const int32_t* seg_len,
                const int32_t* quota, const int32_t* n_seg, int32_t* kept_idx,
                int32_t* n_kept, void* stream);
 
-/* Step 6: gather K, V and the post-EMA credit at the kept slots. */
+/* Step 6: gather K, V and the post-EMA credit at the kept slots.
+ * Defined by AMS, Method, Key design 4 (physical compaction into a fixed-length
+ * per-head cache, not a mask) and Key design 1 (the credit stays aligned with
+ * the slots it describes, so it follows the same indices).
+ *   k_out, v_out  [L][B][H][budget][d] bf16 out; credit_out [L][B][H][budget]
+ *   fp32 out; rows past n_kept are zero.  k_out/v_out must not alias k/v.
+ * An index outside [0, T) writes a zero row and sets KVC_STATUS_BAD_INDEX. */
 int kvc_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v,
                 const float* credit_post, int T, const int32_t* kept_idx,
                 const int32_t* n_kept, uint16_t* k_out, uint16_t* v_out,
@@ -194,7 +232,11 @@ int kvc_redundancy_score(kvc_handle* h, const uint16_t* k, const float* score, i
                          const int32_t* pad, float* sel_score, float* redundancy,
                          void* stream);
 
-/* The whole event, steps 1-6, with the intermediates in the workspace.  With
+/* The whole event, steps 1-6, with the intermediates in the workspace.
+ * Defined by AMS, Method, Key designs 1-4 in order (usage and mass, cut points,
+ * quotas and must-keep, in-segment selection and physical compaction), with the
+ * RefreshKV A2/A6 score, exactly as the stage entry points above chain them;
+ * the arguments are those of kvc_mass and kvc_compact.  With
  * cfg.redundancy_sigma > 0, step 5 selects on kvc_redundancy_score's mix. */
 int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
               const uint16_t* v, int T, const int32_t* pad,
@@ -335,10 +377,14 @@ int kvc_profile_read(kvc_handle* h, kvc_kernel_time* out, int capacity,
  * on fewer sequences then.  The config fields kvc_mass uses are checked as in
  * kvc_create; q, k, pad, n_carry, credit_in, credit_post, mass, score are as in
  * kvc_mass.
- * status: optional device uint32 the kernels OR their KVC_STATUS_* bits into
- * (caller-zeroed); NULL uses a word in the scratch that each call clears.
+ * status: device uint32 (required; NULL returns KVC_ERR_ARG) that the kernels
+ * OR their KVC_STATUS_* bits into; the caller zeroes it and reads it after the
+ * stream completes.
  * The first call on a device (with it current) looks up the scratch address
- * with cudaGetSymbolAddress; make that first call before any stream capture.
+ * with cudaGetSymbolAddress and caches it per device; make that first call
+ * before any stream capture.  The cached address belongs to the device's
+ * primary context: after cudaDeviceReset on that device, do not call this
+ * entry point on it again in the same process.
  * Every call shares the scratch: calls that overlap on the GPU race. */
 #define KVC_NOALLOC_SCRATCH_FLOATS (1u << 20)
 int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const uint16_t* k,

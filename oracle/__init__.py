@@ -19,6 +19,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass
 
 import numpy as np
@@ -138,6 +139,26 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
+def _over_units(fn, p, arrays, threads):
+    """Run ``fn(p, *chunk)`` on contiguous chunks of units in a thread pool and
+    join the results along the unit axis.  Every array in ``arrays`` is unit-major
+    ([U, ...]).  Units are independent, and ctypes releases the GIL for the
+    duration of each C call, so the chunks run on separate cores; the arithmetic
+    is the same single-unit code either way."""
+    U = len(arrays[0])
+    threads = max(1, min(int(threads), U))
+    bounds = np.linspace(0, U, threads + 1).astype(int)
+
+    def run(i):
+        return fn(p, *[np.asarray(a)[bounds[i]:bounds[i + 1]] for a in arrays])
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(run, range(threads)))
+    if isinstance(parts[0], dict):
+        return {k: np.concatenate([q[k] for q in parts], axis=0) for k in parts[0]}
+    return tuple(np.concatenate([q[j] for q in parts], axis=0) for j in range(len(parts[0])))
+
+
 # ---- per-unit fp64 steps (used by the pins) ---------------------------------
 
 def usage(q: np.ndarray, k: np.ndarray, pad: int = 0, scale: float | None = None):
@@ -252,8 +273,11 @@ def s_max(p: RefParams, T: int) -> int:
     return lib().kvc_ref_s_max(ctypes.byref(cfg), T)
 
 
-def mass(p: RefParams, q_bits, k_bits, credit_in, pad, n_carry):
-    """q_bits [U,G,W,d] uint16, k_bits [U,T,d] uint16, credit_in [U,T] f32, pad/n_carry [U]."""
+def mass(p: RefParams, q_bits, k_bits, credit_in, pad, n_carry, threads: int = 1):
+    """q_bits [U,G,W,d] uint16, k_bits [U,T,d] uint16, credit_in [U,T] f32, pad/n_carry [U].
+    threads > 1 splits the units over that many host threads."""
+    if threads > 1:
+        return _over_units(mass, p, (q_bits, k_bits, credit_in, pad, n_carry), threads)
     q_bits = _c(q_bits, np.uint16)
     k_bits = _c(k_bits, np.uint16)
     U, T = k_bits.shape[0], k_bits.shape[1]
@@ -269,7 +293,9 @@ def mass(p: RefParams, q_bits, k_bits, credit_in, pad, n_carry):
     return m, s, c
 
 
-def segment_quota(p: RefParams, mass_f32, pad):
+def segment_quota(p: RefParams, mass_f32, pad, threads: int = 1):
+    if threads > 1:
+        return _over_units(segment_quota, p, (mass_f32, pad), threads)
     mass_f32 = _c(mass_f32, np.float32)
     U, T = mass_f32.shape
     pad = _c(pad, np.int32)
@@ -284,7 +310,9 @@ def segment_quota(p: RefParams, mass_f32, pad):
     return st, ln, qu, ns
 
 
-def select(p: RefParams, score_f32, pad, seg_start, seg_len, quota, n_seg):
+def select(p: RefParams, score_f32, pad, seg_start, seg_len, quota, n_seg, threads: int = 1):
+    if threads > 1:
+        return _over_units(select, p, (score_f32, pad, seg_start, seg_len, quota, n_seg), threads)
     score_f32 = _c(score_f32, np.float32)
     U, T = score_f32.shape
     kept = np.zeros((U, p.budget), np.int32)
@@ -339,10 +367,13 @@ def redundancy_score(k_bits, score, pad, sigma):
     return f, R, r
 
 
-def event(p: RefParams, q_bits, k_bits, v_bits, credit_in, pad, n_carry):
+def event(p: RefParams, q_bits, k_bits, v_bits, credit_in, pad, n_carry, threads: int = 1):
     """The whole event, steps 1-6, for U units. Returns a dict of numpy arrays.
     With p.redundancy_sigma > 0 step 5 selects on the SkipKV redundancy-mixed
-    score (rounded to fp32, the score's own precision); "sel_score" holds it."""
+    score (rounded to fp32, the score's own precision); "sel_score" holds it.
+    threads > 1 splits the units over that many host threads."""
+    if threads > 1:
+        return _over_units(event, p, (q_bits, k_bits, v_bits, credit_in, pad, n_carry), threads)
     m, s, c = mass(p, q_bits, k_bits, credit_in, pad, n_carry)
     st, ln, qu, ns = segment_quota(p, m, pad)
     sel = s

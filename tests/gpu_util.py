@@ -8,6 +8,7 @@ import torch
 
 import eviction_gb300 as kvc
 import workload as wl
+from tests import e2e_check
 
 
 def config_for(w: wl.Workload, T: int, **kw) -> kvc.Config:
@@ -82,67 +83,6 @@ def gpu_event(h: kvc.Handle, g, T):
     return out
 
 
-def mass_close(gpu, ref, rtol=1e-4, atol=1e-9):
-    """|gpu - ref| <= rtol*|ref| + atol elementwise; returns (ok, worst relative error)."""
-    finite = np.isfinite(ref)
-    with np.errstate(invalid="ignore"):
-        err = np.abs(gpu.astype(np.float64) - ref.astype(np.float64))
-    bound = rtol * np.abs(ref.astype(np.float64)) + atol
-    ok = bool(np.all(err[finite] <= bound[finite])) and bool(
-        np.array_equal(gpu[~finite], ref[~finite]))
-    rel = float(np.max(err[finite] / np.maximum(np.abs(ref[finite]), 1e-30))) if finite.any() else 0.0
-    return ok, rel
-
-
-def check_unit_e2e(p, w: wl.Workload, pad_u: int, kept_g, mass_g, score_g, seg_g, r, i):
-    """One unit's end-to-end result against oracle run `r` (row i).
-
-    kept_g: the GPU's kept slots (ascending); mass_g / score_g: the GPU's fp32
-    m_used and score; seg_g: the GPU's segments for the unit (dict with
-    seg_start, seg_len, quota rows and n_seg) from its own segment kernel on its
-    own mass.  Nothing from the GPU is fed to the oracle.  Checks:
-      1. m_used and score within 1e-4 relative (+1e-9) of the oracle's;
-      2. identical kept sets, or, where the GPU's segments and quotas equal the
-         oracle's, kept sets that differ only by swapped pairs at score near-ties
-         (gap at most 1e-5 of G*W, the total usage scale);
-      3. where the segments differ, the oracle's own fp64 cumulative mass lies
-         within 1e-5 of a cut threshold k*delta at the first differing boundary
-         (a rounding-order shift inside the mass tolerance); where only quotas
-         differ, at most two units moved between segments.
-    Returns "identical", "near_tie" or "shifted".
-    """
-    ok_m, rel_m = mass_close(mass_g, r["mass"][i])
-    ok_s, rel_s = mass_close(score_g, r["score"][i])
-    assert ok_m and ok_s, f"unit row {i}: mass rel {rel_m:.3g}, score rel {rel_s:.3g}"
-    kept_r = r["kept_idx"][i, :r["n_kept"][i]]
-    if np.array_equal(kept_r, kept_g):
-        return "identical"
-    ns_g, ns_r = int(seg_g["n_seg"]), int(r["n_seg"][i])
-    st_g, st_r = seg_g["seg_start"][:ns_g], r["seg_start"][i, :ns_r]
-    same_seg = ns_g == ns_r and np.array_equal(st_g, st_r) and np.array_equal(
-        seg_g["seg_len"][:ns_g], r["seg_len"][i, :ns_r])
-    a, b = set(kept_g.tolist()), set(kept_r.tolist())
-    only_g, only_r = sorted(a - b), sorted(b - a)
-    assert len(only_g) == len(only_r)
-    if same_seg and np.array_equal(seg_g["quota"][:ns_g], r["quota"][i, :ns_r]):
-        s = r["score"][i]
-        gap = max(abs(float(s[x]) - float(s[y])) for x, y in zip(only_g, only_r))
-        tol = 1e-5 * w.group * w.window
-        assert gap <= tol, f"unit row {i}: kept sets differ beyond near-ties ({gap:.3g})"
-        return "near_tie"
-    if same_seg:
-        moved = int(np.abs(seg_g["quota"][:ns_g] - r["quota"][i, :ns_r]).sum())
-        assert moved <= 4, f"unit row {i}: quotas differ by {moved} units"
-        return "shifted"
-    # first differing segment start, in valid-slot offsets
-    n = min(ns_g, ns_r)
-    k0 = next((k for k in range(n) if st_g[k] != st_r[k]), n)
-    cuts = sorted({int(st_g[k0]) if k0 < ns_g else int(mass_g.shape[0]),
-                   int(st_r[k0]) if k0 < ns_r else int(mass_g.shape[0])})
-    m = r["mass"][i][pad_u:].astype(np.float64)
-    cum = np.cumsum(m) / m.sum()
-    lo, hi = max(cuts[0] - pad_u - 2, 0), min(cuts[1] - pad_u + 1, len(cum))
-    levels = np.arange(1, int(1.0 / p.delta) + 1) * p.delta
-    near = np.min(np.abs(cum[lo:hi, None] - levels[None, :])) if hi > lo else 1.0
-    assert near <= 1e-5, f"unit row {i}: segments differ away from a cut threshold ({near:.3g})"
-    return "shifted"
+# the end-to-end checker lives in its own module (CPU-tested in test_e2e_check.py)
+mass_close = e2e_check.mass_close
+check_unit_e2e = e2e_check.check_unit_e2e

@@ -84,26 +84,26 @@ def test_segments_quotas_select_bit_exact(ref, runs, name, sw):
 
 @pytest.mark.parametrize("sw", list(SWITCHES))
 def test_event_end_to_end(ref, runs, sw):
+    """The event under each switch against the oracle's chain through the
+    end-to-end checker (GPU segments from the GPU's own mass)."""
     import eviction_gb300 as kvc
     w, inp, kw, r = runs[("qwen_small", sw)]
+    p = gu.ref_params(ref, w, **kw)
     T = inp.T
     h = kvc.Handle(gu.config_for(w, T, **kw))
-    out = gu.gpu_event(h, gu.to_device(inp), T)
+    g = gu.to_device(inp)
+    out = gu.gpu_event(h, g, T)
+    m, s, _ = gu.gpu_mass(h, g, T)
+    st, ln, qu, ns = gu.gpu_segment_quota(h, m, inp.pad.numpy(), T)
     assert h.device_status() == 0
     U = w.units
     kept = out["kept_idx"].reshape(U, -1).cpu().numpy()
     nk = out["n_kept"].reshape(U).cpu().numpy()
     assert np.array_equal(nk, r["n_kept"])
-    tol = 1e-5 * w.group * w.window
+    pads_u = wl.unit_pad(inp).numpy()
     for u in range(U):
-        a = set(kept[u, :nk[u]].tolist())
-        b = set(r["kept_idx"][u, :nk[u]].tolist())
-        if a == b:
-            continue
-        only_gpu, only_ref = sorted(a - b), sorted(b - a)
-        s = r["score"][u]
-        gap = max(abs(float(s[x]) - float(s[y])) for x, y in zip(only_gpu, only_ref))
-        assert gap <= tol, f"unit {u}: kept sets differ beyond near-ties ({gap:.3g})"
+        seg = dict(seg_start=st[u], seg_len=ln[u], quota=qu[u], n_seg=int(ns[u]))
+        gu.check_unit_e2e(p, w, int(pads_u[u]), kept[u, :nk[u]], m[u], s[u], seg, r, u)
 
 
 def test_switches_change_the_result(runs):

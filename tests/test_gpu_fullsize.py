@@ -2,22 +2,27 @@
 benchmark times, checked on sampled units that the oracle recomputes one by one.
 
   * qwen_1l (32 units): every unit;
-  * qwen_28l (3584 units): 6 sampled units through the 4-event chain (credit
-    carried, 512 fresh slots appended per event). The oracle runs its own chain
-    from its own compacted caches, so it never takes a CUDA output as input; a
-    unit whose kept set differs from the oracle's (near-tie or shifted cut)
-    leaves the chain comparison from then on;
-  * llama_ragged (16384 units, left padded to the longest sequence): sampled
-    short and long sequences; then the same sequences regrouped by length in
-    groups of 8 (less padding, same valid data) must keep the same slots up to
-    the padding shift, and every unit where the two runs differ is checked
-    against the oracle on both layouts;
-  * long (T = 32768, 448 units): 2 sampled units.
+  * qwen_28l (3584 units): 64 seeded random units over all 28 layers through
+    the 4-event chain (credit carried, 512 fresh slots appended per event). The
+    oracle runs its own chain from its own compacted caches, so it never takes
+    a CUDA output as input; a unit whose kept set differs from the oracle's
+    (a knife-edge difference the checker accepted) no longer holds the same
+    cache as the oracle's chain, so it leaves the comparison from then on, and
+    at least 7 in 8 of the units must stay identical through all four events;
+  * llama_ragged (16384 units, left padded to the longest sequence): 32 sampled
+    units over short and long sequences; then the same sequences regrouped by
+    length in groups of 8 (less padding, same valid data) must keep the same
+    slots up to the padding shift, and every unit where the two runs differ is
+    checked against the oracle on both layouts;
+  * long (T = 32768, 448 units): 8 sampled units.
+Every test prints how many units got each verdict of the checker.
 Per unit (tests.gpu_util.check_unit_e2e): mass and score within 1e-4 relative,
 and the oracle's own kept set matches the GPU's up to near-ties or a cut that
 moved at a threshold (GPU segments from the GPU's own kernel; no GPU value is
 ever an oracle input); compaction is exact for the GPU's indices.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -27,6 +32,14 @@ import workload as wl
 pytestmark = pytest.mark.gpu
 
 from tests import gpu_util as gu  # noqa: E402
+
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+def _tally(label, verdicts):
+    counts = {v: verdicts.count(v) for v in ("identical", "near_tie", "quota_shift", "cut_shift")}
+    print(f"{label}: {len(verdicts)} units checked, verdicts {counts}")
+    return counts
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -108,8 +121,9 @@ def test_qwen_1l_every_unit(ref):
     h = kvc.Handle(gu.config_for(w, inp.T))
     out, st = _run(h, inp)
     units = list(range(w.units))
-    r = ref.event(p, *_unit_inputs(inp, units))
+    r = ref.event(p, *_unit_inputs(inp, units), threads=THREADS)
     v = _check(ref, p, w, inp, out, st, units, r)
+    _tally("qwen_1l", v)
     assert v.count("identical") >= len(units) - 2
 
 
@@ -117,7 +131,9 @@ def test_qwen_28l_four_event_chain(ref):
     import eviction_gb300 as kvc
     w = wl.CONFIGS["qwen_28l"]
     p = gu.ref_params(ref, w)
-    units = [0, 517, 1203, 2048, 2999, w.units - 1]
+    rng = np.random.default_rng(28)
+    units = sorted(rng.choice(w.units, 64, replace=False).tolist())
+    assert len({u // (w.batch * w.n_kv_heads) for u in units}) >= 20   # spread over layers
     inp = wl.generate(w, device="cuda")
     h = kvc.Handle(gu.config_for(w, w.budget + w.interval))
     r_in = _unit_inputs(inp, units)
@@ -125,10 +141,11 @@ def test_qwen_28l_four_event_chain(ref):
     Kb, I = w.budget, w.interval
     for event in range(w.n_events):
         out, st = _run(h, inp)
-        r = ref.event(p, *r_in)
-        v = _check(ref, p, w, inp, out, st, [units[i] for i in alive], r, rows=alive)
+        r = ref.event(p, *r_in, threads=THREADS)
+        v = _check(ref, p, w, inp, out, st, [units[i] for i in alive], r,
+                   rows=alive)
+        _tally(f"qwen_28l event {event + 1}", v)
         alive = [i for i, verdict in zip(alive, v) if verdict == "identical"]
-        assert len(alive) >= len(units) // 2, f"event {event}: {v}"
         if event + 1 == w.n_events:
             break
         nxt = wl.next_event(w, inp, out["k_out"], out["v_out"], out["credit_out"],
@@ -142,6 +159,9 @@ def test_qwen_28l_four_event_chain(ref):
         inp = nxt
         del out, st
         torch.cuda.empty_cache()
+    print(f"qwen_28l: {len(alive)} of {len(units)} units identical through all "
+          f"{w.n_events} events")
+    assert len(alive) >= len(units) * 7 // 8, f"{len(alive)} of {len(units)} stayed identical"
 
 
 def test_llama_ragged_padded_and_grouped(ref):
@@ -154,11 +174,13 @@ def test_llama_ragged_padded_and_grouped(ref):
     out, st = _run(h, inp)
     pads = inp.pad.cpu().numpy()
     order = np.argsort(pads, kind="stable")
-    picks = [(0, int(order[0]), 0), (7, int(order[1]), 3), (19, int(order[len(order) // 2]), 5),
-             (31, int(order[-1]), 7)]
+    rng = np.random.default_rng(64)
+    seqs = list(order[:4]) + list(order[-4:]) + list(rng.choice(order[4:-4], 8, replace=False))
+    picks = [(int(rng.integers(0, w.n_layers)), int(b), int(rng.integers(0, w.n_kv_heads)))
+             for b in seqs for _ in range(2)]
     units = [wl.unit_index(w, l, b, hh) for l, b, hh in picks]
-    r = ref.event(p, *_unit_inputs(inp, units))
-    _check(ref, p, w, inp, out, st, units, r)
+    r = ref.event(p, *_unit_inputs(inp, units), threads=THREADS)
+    _tally("llama_ragged padded", _check(ref, p, w, inp, out, st, units, r))
     kept_pad = out["kept_idx"].cpu()
     nk_pad = out["n_kept"].cpu()
     del out, st
@@ -196,8 +218,9 @@ def test_llama_ragged_padded_and_grouped(ref):
         mine = [d for d in differing if d[4] == g0][:6]
         if mine:
             gunits = [wl.unit_index(gw, l, j, hh) for l, _, hh, j, _ in mine]
-            rg = ref.event(p, *_unit_inputs(gi, gunits))
-            _check(ref, p, gw, gi, out_g, st_g, gunits, rg)
+            rg = ref.event(p, *_unit_inputs(gi, gunits), threads=THREADS)
+            _tally(f"llama_ragged group {g0 // 8} (differing units)",
+                   _check(ref, p, gw, gi, out_g, st_g, gunits, rg))
         del out_g, st_g, gi
         hg.close()
         torch.cuda.empty_cache()
@@ -205,8 +228,10 @@ def test_llama_ragged_padded_and_grouped(ref):
         h = kvc.Handle(gu.config_for(w, T))
         out, st = _run(h, inp)
         units = [wl.unit_index(w, l, b, hh) for l, b, hh, _, _ in differing[:16]]
-        r = ref.event(p, *_unit_inputs(inp, units))
-        _check(ref, p, w, inp, out, st, units, r)
+        r = ref.event(p, *_unit_inputs(inp, units), threads=THREADS)
+        _tally("llama_ragged padded (differing units)", _check(ref, p, w, inp, out, st, units, r))
+    print(f"llama_ragged: {len(differing)} of {w.units} units differ between the padded and "
+          "the grouped layout")
     # padding only changes fp32 reduction order: near-tie flips in a few units
     assert len(differing) <= w.units // 200, f"{len(differing)} units differ"
 
@@ -218,6 +243,6 @@ def test_long_context(ref):
     inp = wl.generate(w, device="cuda")
     h = kvc.Handle(gu.config_for(w, inp.T))
     out, st = _run(h, inp)
-    units = [3, w.units - 2]
-    r = ref.event(p, *_unit_inputs(inp, units))
-    _check(ref, p, w, inp, out, st, units, r)
+    units = sorted(np.random.default_rng(32768).choice(w.units, 8, replace=False).tolist())
+    r = ref.event(p, *_unit_inputs(inp, units), threads=THREADS)
+    _tally("long", _check(ref, p, w, inp, out, st, units, r))

@@ -58,3 +58,31 @@ def test_max_query_rows(ref):
     out, st = _run(h, inp)
     r = ref.event(p, *_unit_inputs(inp, [0]))
     _check(ref, p, w, inp, out, st, [0], r)
+
+
+def test_more_units_than_grid_y(ref):
+    """More than 65535 units (the CUDA limit on a grid's y extent, which the
+    gather's unit axis uses): the gather launches in chunks of units, so units
+    past 65535 are compacted too.  Every unit's compaction is checked against a
+    torch gather of its own kept slots; units on both sides of the limit go
+    through the end-to-end checker against the oracle."""
+    import eviction_gb300 as kvc
+    w = wl.scaled(wl.CONFIGS["qwen_1l"], n_layers=1, batch=16500, n_kv_heads=4, group=1,
+                  head_dim=64, T=48, window=4, budget=24, n_recent=8, regions=(1, 1),
+                  region_len=("uniform", 4, 8))
+    assert w.units > 65535
+    inp = wl.generate(w, device="cuda")
+    p = gu.ref_params(ref, w)
+    h = kvc.Handle(gu.config_for(w, inp.T))
+    out, st = _run(h, inp)
+    U, T, d = w.units, inp.T, w.head_dim
+    kept = out["kept_idx"].reshape(U, -1).long()
+    assert bool((out["n_kept"] == w.budget).all())
+    for name in ("k", "v"):
+        src = getattr(inp, name).reshape(U, T, d)
+        ref_rows = torch.gather(src, 1, kept[:, :, None].expand(-1, -1, d))
+        assert torch.equal(out[f"{name}_out"].reshape(U, -1, d).view(torch.int16),
+                           ref_rows.view(torch.int16)), name
+    units = [0, 65534, 65535, 65536, U - 1]
+    r = ref.event(p, *_unit_inputs(inp, units))
+    _check(ref, p, w, inp, out, st, units, r)

@@ -26,6 +26,7 @@ import workload as wl
 
 pytestmark = pytest.mark.gpu
 
+from tests import e2e_check as ec  # noqa: E402
 from tests import gpu_util as gu  # noqa: E402
 
 U32 = 2.0 ** -24
@@ -275,9 +276,12 @@ def test_event_with_sigma_end_to_end(ref):
         I = s / s.sum()
         tol = 4e-4 * sigma * I.max() + 1e-4 * (1 - sigma) * r["redundancy"][u][pu:].max()
         f = r["sel_score"][u]
-        only_gpu, only_ref = sorted(a - b), sorted(b - a)
-        gap = max(abs(float(f[x]) - float(f[y])) for x, y in zip(only_gpu, only_ref))
-        assert gap <= tol, f"unit {u}: kept sets differ beyond near-ties ({gap:.3g} > {tol:.3g})"
+        ns = int(r["n_seg"][u])
+        gap = ec.cutoff_distance(kept[u, :nk[u]], r["kept_idx"][u, :nk[u]], f, int(pu), T,
+                                 r["seg_start"][u, :ns], r["seg_len"][u, :ns], w.budget,
+                                 w.n_sink, w.n_recent)
+        assert gap <= tol, (f"unit {u}: a slot kept by one side only lies {gap:.3g} from its "
+                            f"segment's cut-off (tolerance {tol:.3g})")
     # sigma really changes the selection
     r0 = ref.event(gu.ref_params(ref, w), *gu.oracle_inputs(inp))
     assert not np.array_equal(r0["kept_idx"], r["kept_idx"])
