@@ -88,6 +88,7 @@ def method_kw(args):
     return kw
 
 
+
 # --------------------------------------------------------------------- helpers
 
 def load_peaks():
@@ -595,14 +596,16 @@ def run_ours(args, w):
             bytes_ev += b * n_u
             for name, (bound, fl, by) in pk.items():
                 acc = per_kernel_work.setdefault(name, [bound, 0.0, 0.0])
-                acc[1] += fl * n_u / len(parts)   # per launch: each part is one launch
-                acc[2] += by * n_u / len(parts)
+                acc[1] += fl * n_u   # per step; divided over the step's launches below
+                acc[2] += by * n_u
     total_kernel_ms = sum(k["total_ms"] for k in kernels) or 1.0
     krows = []
     for k in kernels:
         if not k["launches"]:
             continue
         bound, fl, by = per_kernel_work[k["name"]]
+        per_step = k["launches"] / args.steps   # launches of this kernel in one step
+        fl, by = fl / per_step, by / per_step   # algorithmic work of one launch
         avg_s = k["total_ms"] / k["launches"] / 1000.0
         if bound == "tensor":
             ach, peak, unit = fl / avg_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
@@ -611,13 +614,15 @@ def run_ours(args, w):
         krows.append({"name": k["name"], "launches": k["launches"],
                       "avg_ms": 1000.0 * avg_s, "share": k["total_ms"] / total_kernel_ms,
                       "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
-                      "frac": ach / peak, "algorithmic_per_launch": fl if bound == "tensor" else by})
+                      "frac": ach / peak, "algorithmic_per_launch": fl if bound == "tensor" else by,
+                      "launches_per_step": per_step})
     dom = max(krows, key=lambda r: r["avg_ms"] * r["launches"])
     roofline = {"kernel": dom["name"], "bound": dom["bound"], "achieved": dom["achieved"],
                 "peak": dom["peak"], "unit": dom["unit"], "frac": dom["frac"],
                 "peak_source": f"{'bf16_tflops (burst)' if dom['bound'] == 'tensor' else 'hbm_gbs'}"
                                f" of {peak_src}",
-                "traffic": read_traffic(dom["name"], w.name)}
+                "traffic": (None if read_traffic(dom["name"], w.name) is None else
+                            read_traffic(dom["name"], w.name) / dom["launches_per_step"])}
     t_flop = flops_ev / (peaks["bf16_tflops"] * 1e12)
     t_byte = bytes_ev / (peaks["hbm_gbs"] * 1e9)
     roof_ms = 1000.0 * max(t_flop, t_byte)
