@@ -21,7 +21,7 @@ def lib():
 def _declared(header):
     text = open(os.path.join(ROOT, "include", header)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(kvc_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(kvc_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_lists_all_entry_points():
