@@ -71,6 +71,9 @@ def parse_args():
                     help="compact into a paged KV pool (block size 16) instead of dense caches")
     ap.add_argument("--ablation", choices=sorted(ABLATIONS), default="none",
                     help="time one of the method's ablations (the pages' ablation table)")
+    ap.add_argument("--attn-kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="step-1 tensor-core kernel: 1 = one SM per MMA, 2 = CTA pairs, "
+                         "0 = the library's choice")
     ap.add_argument("--grouped", type=int, default=0, metavar="G",
                     help="ragged batch sorted by length and run in groups of G sequences, each "
                          "padded only to its own longest sequence (SkipKV's batch grouping)")
@@ -78,6 +81,11 @@ def parse_args():
                     help="select on the SkipKV key-redundancy mix with this sigma (0.1 in the "
                          "pages); 0 = the attention score alone")
     return ap.parse_args()
+
+
+def sched_kw(args):
+    """Switches of our arm only that change how, not what, it computes."""
+    return {"attn_kernel": args.attn_kernel} if args.attn_kernel else {}
 
 
 def method_kw(args):
@@ -443,7 +451,7 @@ def run_ours(args, w):
     T = first.T
     cfg = kvc.Config(w.n_layers, w.batch, w.n_kv_heads, w.group, w.head_dim,
                      max(T, w.budget + w.interval), w.budget, window=w.window, n_sink=w.n_sink,
-                     n_recent=w.n_recent, **method_kw(args))
+                     n_recent=w.n_recent, **method_kw(args), **sched_kw(args))
     h = kvc.Handle(cfg)
     inp = first
     if w.n_events > 1:
@@ -466,7 +474,7 @@ def run_ours(args, w):
         h.close()
         h = kvc.Handle(kvc.Config(w.n_layers, args.grouped, w.n_kv_heads, w.group, w.head_dim,
                                   T, w.budget, window=w.window, n_sink=w.n_sink,
-                                  n_recent=w.n_recent, **method_kw(args)))
+                                  n_recent=w.n_recent, **method_kw(args), **sched_kw(args)))
         parts = []
         for g0 in range(0, w.batch, args.grouped):
             grp = by_len[g0:g0 + args.grouped]

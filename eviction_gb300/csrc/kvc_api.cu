@@ -100,7 +100,9 @@ int run_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T, const i
   std::string err;
   for (int pass = 1; pass <= 2; ++pass) {
     cudaEvent_t b = mark_begin(h, s);
-    cudaError_t e = kvc::launch_attention_usage(h, a, pass, s, &err);
+    cudaError_t e = h->cfg.attn_kernel == 2
+                        ? kvc::launch_attention_usage_pair(h, a, pass, s, &err)
+                        : kvc::launch_attention_usage(h, a, pass, s, &err);
     if (e != cudaSuccess)
       return err.empty() ? cuda_fail(h, e, "attention usage") : fail(h, KVC_ERR_CUDA, err);
     mark_end(h, pass == 1 ? kvc::kKernelUsagePass1 : kvc::kKernelUsagePass2, b, s);
@@ -249,6 +251,7 @@ int validate_config(const kvc_config* c, std::string* why) {
     return bad("quota_by_len and global_topk must be 0 or 1");
   if (!(c->redundancy_sigma >= 0.f && c->redundancy_sigma <= 1.f))
     return bad("redundancy_sigma must lie in [0, 1] (0 = off)");
+  if (c->attn_kernel < 0 || c->attn_kernel > 2) return bad("attn_kernel must be 0, 1 or 2");
   if (c->head_dim != 64 && c->head_dim != 128) {
     *why = "head_dim must be 64 or 128";
     return KVC_ERR_UNSUPPORTED;

@@ -110,6 +110,10 @@ struct UsageArgs {
 cudaError_t launch_attention_usage(const kvc_handle* h, const UsageArgs& a,
                                    int pass, cudaStream_t s, std::string* err);
 
+// The same pass on CTA pairs (cta_group::2, M256 x N128), attn_usage_pair.cu.
+cudaError_t launch_attention_usage_pair(const kvc_handle* h, const UsageArgs& a,
+                                        int pass, cudaStream_t s, std::string* err);
+
 cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
                              const int32_t* n_carry, const float* credit_in,
                              float* credit_post, float* mass, float* score,
@@ -267,6 +271,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_now(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_wait, but polling without suspending the thread, with the same time
+// limit and abort flag (checked every 256 polls).
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, uint32_t* status) {
+  if (mbar_test_now(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test_now(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(status, KVC_STATUS_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // 2-D tiled TMA load global -> shared, completion on `bar` (transaction bytes).
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
                                             int x, int y, uint64_t* bar) {
@@ -420,6 +456,106 @@ __device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32],
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
         "=r"(r[30]), "=r"(r[31]), "=f"(mx)
       : "r"(taddr)
+      : "memory");
+}
+
+// ---- CTA pairs (cluster of two CTAs sharing one MMA: tcgen05 .cta_group::2) ----
+// Every tcgen05 instruction of a kernel uses the same .cta_group, so a paired
+// kernel allocates, issues and commits with these forms only.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared::cluster address of the object at local shared address `local` in
+// the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// All threads of both CTAs: release this CTA's prior shared-memory writes
+// (barrier inits included) to the cluster, then wait for the peer.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// Arrive once on an mbarrier given by its shared::cluster address (this CTA's
+// or the peer's).  Default semantics (release at CTA scope): a cluster-scope
+// release would be a full memory barrier on every call, and the hazard it
+// guards here -- this warp's tensor-memory reads against the next MMA's
+// writes -- is ordered by tcgen05.fence::before_thread_sync before the arrive.
+#ifndef KVC_REMOTE_ARRIVE_RELAXED
+#define KVC_REMOTE_ARRIVE_RELAXED 0
+#endif
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+#if KVC_REMOTE_ARRIVE_RELAXED
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+#else
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+#endif
+}
+
+// 3-D tiled TMA load into this CTA's shared memory whose completion (bytes)
+// is counted on the mbarrier at shared::cluster address `bar` -- the pair's
+// leading CTA's barrier, for the operands its MMA reads from both CTAs.
+__device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// One warp of EACH CTA of the pair executes these together: the columns are
+// allocated at the same address in both CTAs' tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D[M x N] (+)= A * B^T over both CTAs: each CTA holds M/2 rows of A and N/2
+// rows of B at the same shared-memory offsets and receives its M/2 rows of D
+// at the same tensor-memory address.  Issued by one thread of the leading CTA.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at local offset `bar` in every CTA of `cta_mask`
+// when all tcgen05 ops this thread issued so far are done.
+__device__ __forceinline__ void mma_commit_pair_multicast(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// As above, on this CTA's own barrier only.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
       : "memory");
 }
 

@@ -142,7 +142,8 @@ extern "C" int kvc_mass_noalloc(const kvc_config* cfg, const uint16_t* q, const 
                                              : 1.0 / std::sqrt(static_cast<double>(d.d));
   kvc::UsageArgs a{q, k, pad, T, static_cast<float>(sc * 1.4426950408889634)};
   for (int pass = 1; pass <= 2; ++pass) {
-    e = kvc::launch_attention_usage(&h, a, pass, s, nullptr);
+    e = cfg->attn_kernel == 2 ? kvc::launch_attention_usage_pair(&h, a, pass, s, nullptr)
+                              : kvc::launch_attention_usage(&h, a, pass, s, nullptr);
     if (e != cudaSuccess) {
       std::fprintf(stderr, "kvc_mass_noalloc: attention kernels: %s\n", cudaGetErrorString(e));
       cudaGetLastError();

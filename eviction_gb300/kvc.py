@@ -49,7 +49,7 @@ class _CConfig(ctypes.Structure):
                 ("lambda_", ctypes.c_float), ("beta", ctypes.c_float), ("eps", ctypes.c_float),
                 ("softmax_scale", ctypes.c_float), ("seg_fixed", ctypes.c_int),
                 ("quota_by_len", ctypes.c_int), ("global_topk", ctypes.c_int),
-                ("redundancy_sigma", ctypes.c_float)]
+                ("redundancy_sigma", ctypes.c_float), ("attn_kernel", ctypes.c_int)]
 
 
 # The ablations of the method's ablation table as Config keyword switches
@@ -90,6 +90,7 @@ class Config:
     quota_by_len: int = 0    # ablation: quotas by segment length instead of mass
     global_topk: int = 0     # ablation: one segment, per-head global top-k
     redundancy_sigma: float = 0.0  # > 0: select on sigma*I - (1-sigma)*R (key redundancy)
+    attn_kernel: int = 0     # step-1 tensor-core kernel: 1 one SM per MMA, 2 CTA pairs, 0 auto (1)
 
     def c(self) -> _CConfig:
         return _CConfig(self.n_layers, self.batch, self.n_kv_heads, self.group, self.head_dim,
@@ -97,7 +98,7 @@ class Config:
                         self.delta, self.seg_min, self.seg_max, self.q_min, self.n_sink,
                         self.n_recent, self.lam, self.beta, self.eps, self.softmax_scale,
                         self.seg_fixed, self.quota_by_len, self.global_topk,
-                        self.redundancy_sigma)
+                        self.redundancy_sigma, self.attn_kernel)
 
     @property
     def units(self):

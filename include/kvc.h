@@ -123,6 +123,14 @@ typedef struct {
    * (see kvc_redundancy_score); 0 = off.  Segments and quotas stay on the
    * attention mass.                                                         */
   float redundancy_sigma;
+  /* Tensor-core kernel of step 1 (same results up to fp32 summation order):
+   * 1 = one SM per MMA (M128 x N256, two accumulators per SM);
+   * 2 = CTA pairs (two SMs of a TPC share each M256 x N128 MMA, four
+   *     accumulators per SM, two MMA-issuing threads);
+   * 0 = automatic (1: the pairs are as fast on the attention pass over
+   *     slots and slower on the one over query rows, whose odd tile count
+   *     leaves half of a pair idle). */
+  int attn_kernel;
 } kvc_config;
 
 typedef struct kvc_handle kvc_handle;
