@@ -42,8 +42,8 @@ from eviction_gb300.kvc import ABLATIONS  # noqa: E402  (the pages' ablations as
 KERNEL_SOURCES = {
     "compact_paged": "paged.cu",
     "refresh_trigger": "refresh.cu",
-    "usage_pass1_rowstats_tcgen05": "attn_usage.cu",
-    "usage_pass2_colsum_tcgen05": "attn_usage.cu",
+    "usage_pass1_rowstats_tcgen05": ("attn_usage.cu", "attn_common.cuh"),
+    "usage_pass2_colsum_tcgen05": ("attn_usage.cu", "attn_common.cuh"),
     "mass_pool_ema": "mass_post.cu",
     "segment_quota": "segment_quota.cu",
     "select_topk": "select.cu",
@@ -137,11 +137,15 @@ def unit_work(w, T_valid, T):
 
 
 def source_sha(kernel):
+    """First 16 hex digits of the sha256 of the kernel's source file(s), concatenated."""
     src = KERNEL_SOURCES.get(kernel)
     if not src:
         return None
-    with open(os.path.join(ROOT, "eviction_gb300", "csrc", src), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in (src if isinstance(src, tuple) else (src,)):
+        with open(os.path.join(ROOT, "eviction_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def read_traffic(kernel, workload):

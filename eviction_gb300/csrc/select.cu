@@ -27,6 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRegPer = 8;  // slots per thread up to which the excess search keeps keys in registers
+constexpr int kKeyPer = 16;  // longer units: gathered pick keys per thread held in registers
 
 enum : uint8_t { kOut = 0, kMust = 1, kPick = 2 };
 
@@ -133,6 +134,8 @@ __global__ void __launch_bounds__(kThreads)
   int32_t* s_start = reinterpret_cast<int32_t*>(sm);             // [S_max] valid offset
   int32_t* s_want = s_start + p.S_max;                            // [S_max]
   uint8_t* flag = reinterpret_cast<uint8_t*>(s_want + p.S_max);  // [T]
+  // [budget] pick keys of the excess search of long units (T > kRegPer * kThreads)
+  uint32_t* s_key = reinterpret_cast<uint32_t*>(flag + ((p.T + 15) & ~15));
   __shared__ int red[kWarps];
   __shared__ int red2[2 * kWarps];
   __shared__ int s_scan[kWarps];
@@ -213,12 +216,57 @@ __global__ void __launch_bounds__(kThreads)
         if (total < excess) x = t;
       }
     } else {
-      for (int bit = 31; bit >= 0; --bit) {
-        const uint32_t t = x | (1u << bit);
-        int cnt = 0;
-        for (int v = lo; v < hi; ++v) cnt += (flag[v] == kPick && score_key(sc, v) < t) ? 1 : 0;
-        if (block_count(cnt, red) < excess) x = t;
+      // long units: the picks' keys (at most the budget) gathered once into
+      // shared memory in slot order, then searched there -- in registers when
+      // there are at most kKeyPer per thread -- instead of every step
+      // re-reading all of this thread's slots from global memory
+      int cnt = 0;
+      for (int v = lo; v < hi; ++v) cnt += flag[v] == kPick ? 1 : 0;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
       }
+      if (lane == 31) s_scan[warp] = incl;
+      __syncthreads();
+      int pos = incl - cnt;
+      for (int w = 0; w < warp; ++w) pos += s_scan[w];
+      int n_pick = 0;
+      for (int w = 0; w < kWarps; ++w) n_pick += s_scan[w];
+      for (int v = lo; v < hi; ++v)
+        if (flag[v] == kPick) s_key[pos++] = score_key(sc, v);
+      __syncthreads();
+      if (n_pick <= kKeyPer * kThreads) {  // CTA-uniform
+        uint32_t key[kKeyPer];
+#pragma unroll
+        for (int i = 0; i < kKeyPer; ++i) {
+          const int j = threadIdx.x + i * kThreads;
+          key[i] = j < n_pick ? s_key[j] : 0xffffffffu;  // never below a threshold
+        }
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t t = x | (1u << bit);
+          unsigned c2 = 0;
+#pragma unroll
+          for (int i = 0; i < kKeyPer; ++i) c2 += key[i] < t ? 1u : 0u;
+          c2 = __reduce_add_sync(0xffffffffu, c2);
+          int* rb = red2 + (bit & 1) * kWarps;
+          if (lane == 0) rb[warp] = static_cast<int>(c2);
+          __syncthreads();
+          int total = 0;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) total += rb[w];
+          if (total < excess) x = t;
+        }
+      } else {
+        for (int bit = 31; bit >= 0; --bit) {
+          const uint32_t t = x | (1u << bit);
+          int c2 = 0;
+          for (int j = threadIdx.x; j < n_pick; j += kThreads) c2 += s_key[j] < t ? 1 : 0;
+          if (block_count(c2, red) < excess) x = t;
+        }
+      }
+      __syncthreads();  // s_scan is reused below
     }
     int lt = 0, ties = 0;
     for (int v = lo; v < hi; ++v) {
@@ -278,7 +326,8 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 size_t select_smem_bytes(const kvc_config& c, int T) {
-  return static_cast<size_t>(s_max_of(c, T)) * 8 + static_cast<size_t>(T) + 16;
+  const size_t base = static_cast<size_t>(s_max_of(c, T)) * 8 + ((static_cast<size_t>(T) + 15) & ~size_t(15));
+  return base + (T > kRegPer * kThreads ? static_cast<size_t>(c.budget) * 4 : 0) + 16;
 }
 
 cudaError_t launch_select(const kvc_handle* h, const float* score, int T,
