@@ -27,6 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 
+template <int NT = kThreads>
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -36,15 +37,16 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   __syncthreads();
   float t = 0.f;
   if (threadIdx.x < 32) {
-    t = (lane < kThreads / 32) ? red[lane] : 0.f;
+    t = (lane < NT / 32) ? red[lane] : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (lane == 0) red[kThreads / 32] = t;
+    if (lane == 0) red[NT / 32] = t;
   }
   __syncthreads();
-  return red[kThreads / 32];
+  return red[NT / 32];
 }
 
+template <int NT = kThreads>
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -53,13 +55,13 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   if (lane == 0) red[warp] = v;
   __syncthreads();
   if (threadIdx.x < 32) {
-    float t = (lane < kThreads / 32) ? red[lane] : -INFINITY;
+    float t = (lane < NT / 32) ? red[lane] : -INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-    if (lane == 0) red[kThreads / 32] = t;
+    if (lane == 0) red[NT / 32] = t;
   }
   __syncthreads();
-  return red[kThreads / 32];
+  return red[NT / 32];
 }
 
 struct PostParams {
@@ -77,9 +79,13 @@ struct PostParams {
   float* score;
 };
 
-__global__ void __launch_bounds__(kThreads)
+// Units longer than kSmemT slots sweep global memory.  They are few (a long
+// cache holds few sequences), so each takes a CTA of NT = 1024 threads: four
+// times the loads in flight per unit of a 256-thread CTA.
+template <int NT>
+__global__ void __launch_bounds__(NT)
     mass_post_kernel(PostParams p) {
-  __shared__ float red[kThreads / 32 + 1];
+  __shared__ float red[NT / 32 + 1];
   const int u = blockIdx.x;
   const int b = (u / p.H) % p.B;
   const int T = p.T;
@@ -92,7 +98,7 @@ __global__ void __launch_bounds__(kThreads)
   const float* cin = p.credit_in + base;
 
   if (pad >= T) {
-    for (int i = threadIdx.x; i < T; i += kThreads) {
+    for (int i = threadIdx.x; i < T; i += NT) {
       mass[i] = 0.f;
       score[i] = -INFINITY;
       cpost[i] = 0.f;
@@ -102,13 +108,13 @@ __global__ void __launch_bounds__(kThreads)
 
   // fill value = largest probability of any present row (absent rows hold 0)
   float pm = 0.f;
-  for (int r = threadIdx.x; r < p.R; r += kThreads)
+  for (int r = threadIdx.x; r < p.R; r += NT)
     pm = fmaxf(pm, p.pmax[static_cast<size_t>(u) * p.Rp + r]);
-  const float fill = block_max(pm, red);
+  const float fill = block_max<NT>(pm, red);
 
   // a'(i) = a(i) + fill * (#present (head, query) pairs that cannot see i)
   const int j_lo = max(0, pad - (T - p.W));  // first present window query
-  for (int i = pad + threadIdx.x; i < T; i += kThreads) {
+  for (int i = pad + threadIdx.x; i < T; i += NT) {
     const int unseen = max(0, min(p.W, i - T + p.W) - j_lo) * p.G;
     a[i] += fill * static_cast<float>(unseen);
   }
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(kThreads)
   const int ra = p.avg_pool / 2, rm = p.max_pool / 2;
   const float inv_k = 1.0f / static_cast<float>(p.avg_pool);
   float tot = 0.f;
-  for (int i = threadIdx.x; i < T; i += kThreads) {
+  for (int i = threadIdx.x; i < T; i += NT) {
     if (i < pad) {
       score[i] = -INFINITY;
       continue;
@@ -130,13 +136,13 @@ __global__ void __launch_bounds__(kThreads)
     for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
     tot += fmaxf(s * inv_k, 0.f) + p.eps;
   }
-  const float total1 = block_sum(tot, red);
+  const float total1 = block_sum<NT>(tot, red);
 
   // mass and credit
   const int n_carry = min(max(p.n_carry[b], 0), T - pad);
   const float lam = p.lambda;
   float ctot = 0.f;
-  for (int i = threadIdx.x; i < T; i += kThreads) {
+  for (int i = threadIdx.x; i < T; i += NT) {
     if (i < pad) {
       mass[i] = 0.f;
       cpost[i] = 0.f;
@@ -151,20 +157,20 @@ __global__ void __launch_bounds__(kThreads)
     cpost[i] = c;
     ctot += c;
   }
-  const float c_total = block_sum(ctot, red);
+  const float c_total = block_sum<NT>(ctot, red);
 
   // mix and normalise
   const float beta = p.beta;
   float mtot = 0.f;
-  for (int i = pad + threadIdx.x; i < T; i += kThreads) {
+  for (int i = pad + threadIdx.x; i < T; i += NT) {
     const float m = mass[i];
     const float cn = (c_total > 0.f) ? cpost[i] / c_total : m;
     const float mix = beta * m + (1.0f - beta) * cn;
     mass[i] = mix;
     mtot += mix;
   }
-  const float mix_total = block_sum(mtot, red);
-  for (int i = pad + threadIdx.x; i < T; i += kThreads) mass[i] = mass[i] / mix_total;
+  const float mix_total = block_sum<NT>(mtot, red);
+  for (int i = pad + threadIdx.x; i < T; i += NT) mass[i] = mass[i] / mix_total;
 }
 
 // Units of up to kSmemT slots: one pass.  The filled usage of the unit sits in
@@ -326,7 +332,7 @@ cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
   else if (T <= kSmemT)
     mass_post_smem_kernel<kSmemT / kThreads><<<dm.U, kThreads, 0, s>>>(p);
   else
-    mass_post_kernel<<<dm.U, kThreads, 0, s>>>(p);
+    mass_post_kernel<1024><<<dm.U, 1024, 0, s>>>(p);
   return cudaGetLastError();
 }
 

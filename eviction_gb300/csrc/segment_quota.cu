@@ -204,9 +204,13 @@ __device__ void take_best_bids(const int64_t* rem, const int32_t* ref, int32_t* 
   }
 }
 
-// 12 CTAs per SM (40 registers) rather than 10 at the natural 48: the kernel
-// is latency-bound per unit, and more units in flight shorten the launch.
-__global__ void __launch_bounds__(kThreads, 12)
+// NT = 128: 12 CTAs per SM (40 registers) rather than 10 at the natural 48:
+// the kernel is latency-bound per unit, and more units in flight shorten the
+// launch.  Units longer than 4096 slots are few, and each takes NT = 512
+// threads: a quarter of the slots per thread in the scan and the searches.
+// Every result is exact integer arithmetic, the same for any NT.
+template <int NT>
+__global__ void __launch_bounds__(NT, NT == 128 ? 12 : 3)
     segment_quota_kernel(SegParams p) {
   extern __shared__ uint8_t sm[];
   // dynamic shared layout: seg mass (u64) | rem (i64) | start | len | quota |
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 12)
   int32_t* s_floor = s_q + p.S_cap;
   __shared__ int32_t s_b[kMaxK];
   __shared__ uint64_t s_tau[kMaxK];
-  __shared__ uint64_t s_warp[kThreads / 32];
+  __shared__ uint64_t s_warp[NT / 32];
   __shared__ uint64_t s_total;
   __shared__ int s_nseg;
 
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 12)
   int32_t* o_q = p.quota + static_cast<size_t>(u) * p.S_max;
 
   if (n <= 0) {
-    for (int s = threadIdx.x; s < p.S_max; s += kThreads) {
+    for (int s = threadIdx.x; s < p.S_max; s += NT) {
       o_start[s] = 0;
       o_len[s] = 0;
       o_q[s] = 0;
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 12)
   }
 
   // ---- 1. prefix sums of the fixed-point mass over contiguous thread ranges
-  const int per = (n + kThreads - 1) / kThreads;
+  const int per = (n + NT - 1) / NT;
   const int lo = min(n, threadIdx.x * per), hi = min(n, lo + per);
   uint64_t local = 0;
   for (int v = lo; v < hi; ++v) local += fixed_mass(m[v]);
@@ -255,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 12)
   __syncthreads();
   if (threadIdx.x == 0) {
     uint64_t run = 0;
-    for (int w = 0; w < kThreads / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
       const uint64_t t = s_warp[w];
       s_warp[w] = run;
       run += t;
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 12)
   // is computed once (fp64 is slow on this part), then found by the thread
   // whose range holds it
   const double S_d = __ull2double_rn(S);
-  for (int k = threadIdx.x; k < p.K; k += kThreads) {
+  for (int k = threadIdx.x; k < p.K; k += NT) {
     const double frac = __dmul_rn(static_cast<double>(k + 1), p.delta);
     s_tau[k] = static_cast<uint64_t>(ceil(__dmul_rn(frac, S_d)));
   }
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 12)
   const int ns = s_nseg;
 
   // ---- 4. segment masses (one warp per segment)
-  for (int s = warp; s < ns; s += kThreads / 32) {
+  for (int s = warp; s < ns; s += NT / 32) {
     uint64_t acc = 0;
     for (int v = s_start[s] + lane; v < s_start[s] + s_len[s]; v += 32)
       acc += fixed_mass(m[v]);
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 12)
 
   // ablation: quotas in proportion to segment length (lengths replace masses)
   if (p.quota_by_len)
-    for (int s = threadIdx.x; s < ns; s += kThreads) s_mass[s] = static_cast<uint64_t>(s_len[s]);
+    for (int s = threadIdx.x; s < ns; s += NT) s_mass[s] = static_cast<uint64_t>(s_len[s]);
   __syncthreads();
 
   // ---- 5. quotas (warp 0)
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 12)
   __syncthreads();
 
   // ---- 6. outputs (absolute starts), zero past n_seg
-  for (int s = threadIdx.x; s < p.S_max; s += kThreads) {
+  for (int s = threadIdx.x; s < p.S_max; s += NT) {
     if (s < ns) {
       o_start[s] = pad + s_start[s];
       o_len[s] = s_len[s];
@@ -529,13 +533,14 @@ cudaError_t launch_segment_quota(const kvc_handle* h, const float* mass, int T,
   p.quota = quota;
   p.n_seg = n_seg;
   const size_t smem = segment_smem_bytes(c, T);
+  const bool wide = T > 4096;
+  auto kern = wide ? segment_quota_kernel<512> : segment_quota_kernel<kThreads>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(segment_quota_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  segment_quota_kernel<<<h->dims.U, kThreads, smem, s>>>(p);
+  kern<<<h->dims.U, wide ? 512 : kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
