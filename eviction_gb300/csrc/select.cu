@@ -24,8 +24,7 @@
 namespace kvc {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kThreads = 256;  // units up to 4096 slots (see select_kernel)
 constexpr int kRegPer = 8;  // slots per thread up to which the excess search keeps keys in registers
 constexpr int kKeyPer = 16;  // longer units: gathered pick keys per thread held in registers
 
@@ -35,7 +34,9 @@ __device__ __forceinline__ uint32_t score_key(const float* sc, int v) {
   return float_order_key(__ldg(sc + v));
 }
 
+template <int NT>
 __device__ __forceinline__ int block_count(int v, int* red) {
+  constexpr int kWarps = NT / 32;
   v = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(v)));
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   __syncthreads();
@@ -128,8 +129,13 @@ __device__ __forceinline__ void pick_segment_reg(const float* sc, uint8_t* flag,
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(kThreads)
+// NT = 256 threads; units longer than 4096 slots (few, with many segments)
+// take NT = 1024: four times the warps for the per-segment searches.  The
+// selection compares keys only, so the result is the same for any NT.
+template <int NT>
+__global__ void __launch_bounds__(NT)
     select_kernel(SelParams p) {
+  constexpr int kThreads = NT, kWarps = NT / 32;
   extern __shared__ uint8_t sm[];
   int32_t* s_start = reinterpret_cast<int32_t*>(sm);             // [S_max] valid offset
   int32_t* s_want = s_start + p.S_max;                            // [S_max]
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(kThreads)
   }
   for (int v = threadIdx.x; v < n; v += kThreads)
     flag[v] = (v < n_s || v >= n - n_r) ? kMust : kOut;
-  const int total_picks = block_count(want_sum, red);  // (also orders the writes above)
+  const int total_picks = block_count<NT>(want_sum, red);  // (also orders the writes above)
 
   // segment-local picks, one warp per segment
   for (int s = warp; s < ns; s += kWarps) {
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kThreads)
           const uint32_t t = x | (1u << bit);
           int c2 = 0;
           for (int j = threadIdx.x; j < n_pick; j += kThreads) c2 += s_key[j] < t ? 1 : 0;
-          if (block_count(c2, red) < excess) x = t;
+          if (block_count<NT>(c2, red) < excess) x = t;
         }
       }
       __syncthreads();  // s_scan is reused below
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kThreads)
       lt += (k < x) ? 1 : 0;
       ties += (k == x) ? 1 : 0;
     }
-    const int drop_ties = excess - block_count(lt, red);
+    const int drop_ties = excess - block_count<NT>(lt, red);
     // ties above this thread's range (higher slots are dropped first)
     int incl = ties;
 #pragma unroll
@@ -353,13 +359,14 @@ cudaError_t launch_select(const kvc_handle* h, const float* score, int T,
   p.kept_idx = kept_idx;
   p.n_kept = n_kept;
   const size_t smem = select_smem_bytes(c, T);
+  const bool wide = T > 4096;
+  auto kern = wide ? select_kernel<1024> : select_kernel<kThreads>;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
   }
-  select_kernel<<<h->dims.U, kThreads, smem, s>>>(p);
+  kern<<<h->dims.U, wide ? 1024 : kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
