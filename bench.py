@@ -374,9 +374,10 @@ def cpu_oracle_baseline(args, w, parts):
     nxt = 0
 
     def take(n):
-        """Host copies of the next n sampled units: (inputs, valid tokens)."""
+        """Host copies of the next n sampled units (the sample wraps around the
+        workload's units when they run out): (inputs, valid tokens)."""
         nonlocal nxt
-        chosen = [pool[i] for i in order[nxt:nxt + n]]
+        chosen = [pool[order[(nxt + i) % len(pool)]] for i in range(n)]
         nxt += len(chosen)
         cols = [[] for _ in range(6)]
         tokens = 0
@@ -409,7 +410,7 @@ def cpu_oracle_baseline(args, w, parts):
     half = args.cpu_seconds / 2
     done1 = tok1 = 0
     dt1 = 0.0
-    while nxt < len(pool) and (dt1 < half or done1 == 0):
+    while dt1 < half or done1 == 0:
         cols, tokens = take(1)
         dt1 += run(cols, 1)
         done1 += 1
@@ -417,10 +418,10 @@ def cpu_oracle_baseline(args, w, parts):
     rate1 = tok1 / dt1
     cores = host_cores()
     per_unit = dt1 / done1
-    n_all = int(min(len(pool) - nxt, max(cores, cores * half / per_unit)))
-    n_all = max(1, n_all - n_all % cores if n_all >= cores else n_all)
+    n_all = int(max(cores, cores * half / per_unit))
+    n_all -= n_all % cores
     value, used, sample_all = rate1, 1, None
-    if n_all > 0 and nxt < len(pool):
+    if n_all > 0:
         cols, tokens = take(n_all)
         used = min(cores, n_all)
         dtn = run(cols, used)
@@ -428,7 +429,8 @@ def cpu_oracle_baseline(args, w, parts):
         sample_all = f"{n_all} further units on {used} threads ({dtn:.1f} s)"
     return {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
             "single_core_value": rate1,
-            "sample": (f"random units of the timed event (seed 0), same inputs, C oracle in fp64: "
+            "sample": (f"random units of the timed event (seed 0, repeated once all {len(pool)} are "
+                       f"used), same inputs, C oracle in fp64: "
                        f"{done1} units single-threaded ({dt1:.1f} s, value {rate1:.4g} tokens/s)"
                        + (f"; {sample_all} give the value, cores = threads used"
                           if sample_all else "; value = single-threaded"))}
