@@ -85,3 +85,21 @@ def test_event_all_padding(ref):
     assert out["n_kept"][0] == 0 and out["n_seg"][0] == 0
     assert np.all(out["kept_idx"][0] == -1) and not out["k_out"].any()
     assert not out["mass"].any()
+
+
+def test_thread_split_is_the_same_computation(ref):
+    """The batched calls split over host threads (units are independent, the C code
+    runs unit by unit) give exactly the single-threaded results."""
+    w = wl.scaled(wl.CONFIGS["llama_ragged"], n_layers=1, batch=5, n_kv_heads=2, group=2,
+                  head_dim=64, prefill=(20, 200), generated=100, budget=120)
+    inp = wl.generate(w)
+    p = ref.RefParams(group=w.group, head_dim=w.head_dim, window=w.window, budget=w.budget,
+                      n_sink=w.n_sink, n_recent=w.n_recent)
+    args = (wl.bf16_bits(wl.q_units(inp.q, w)), wl.bf16_bits(wl.units_of(inp.k, w)),
+            wl.bf16_bits(wl.units_of(inp.v, w)), wl.units_of(inp.credit, w).numpy(),
+            wl.unit_pad(inp).numpy(), wl.unit_n_carry(inp).numpy())
+    one = ref.event(p, *args)
+    many = ref.event(p, *args, threads=3)
+    assert one.keys() == many.keys()
+    for k in one:
+        assert np.array_equal(one[k], many[k]), k
