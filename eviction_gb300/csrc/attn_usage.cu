@@ -224,20 +224,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ B producer
-    if (lane == 0) {
+    // (all lanes run the loop and wait converged; lane 0 issues the copies)
+    {
       int b_iter = 0;
       bool ok = true;
       for (int kk = 0, item = cta_item(p, 0); ok && item >= 0; item = cta_item(p, ++kk)) {
         const Item it = decode<PASS>(p, item);
         for (int c = 0; c < it.n_ch; ++c) {
           const int s = b_iter % NS;
-          if (!mbar_wait(&empty[s], ((b_iter / NS) & 1) ^ 1, abort, p.status)) {
+          if (!warp_wait(&empty[s], ((b_iter / NS) & 1) ^ 1, abort, p.status)) {
             ok = false;
             break;
           }
           ++b_iter;
-          mbar_arrive_expect_tx(&full[s], ly.b_bytes);
-          tma_load_3d(b_buf + s * ly.b_bytes, &map_b, 0, it.b_row0 + c * BN, 0, &full[s]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], ly.b_bytes);
+            tma_load_3d(b_buf + s * ly.b_bytes, &map_b, 0, it.b_row0 + c * BN, 0, &full[s]);
+          }
         }
       }
       // drain: every issued copy must land before the CTA may exit
@@ -248,8 +251,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kLoaderWarp) {
     // ------------------------------------------- A tiles and row constants
     // A tile slot t is reloaded as soon as the slot's last MMA of the previous
-    // item has completed, while the other slot's MMAs still run.
-    if (lane == 0) {
+    // item has completed, while the other slot's MMAs still run.  (All lanes
+    // run the loop; lane 0 issues the copies.)
+    {
       int a_cnt[kTiles] = {0, 0};
       int rb_iter = 0;
       bool ok = true;
@@ -259,22 +263,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < kTiles; ++t) {
           if (!ok || it.tile[t] < 0) continue;
-          if (!mbar_wait(&aempty[t], (a_cnt[t] & 1) ^ 1, abort, p.status)) {
+          if (!warp_wait(&aempty[t], (a_cnt[t] & 1) ^ 1, abort, p.status)) {
             ok = false;
             continue;
           }
           ++a_cnt[t];
-          mbar_arrive_expect_tx(&afull[t], ly.a_bytes);
-          // one box: 128 rows x all 64-element K blocks, K block outermost
-          tma_load_3d(a_buf + t * ly.a_bytes, &map_a, 0, it.a_row[t], 0, &afull[t]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&afull[t], ly.a_bytes);
+            // one box: 128 rows x all 64-element K blocks, K block outermost
+            tma_load_3d(a_buf + t * ly.a_bytes, &map_a, 0, it.a_row[t], 0, &afull[t]);
+          }
         }
         if (ok && PASS == 2) {
           const int rb = rb_iter & p.rb_shift;
-          if (!mbar_wait(&rbempty[rb], ((rb_iter >> p.rb_shift) & 1) ^ 1, abort, p.status)) break;
+          if (!warp_wait(&rbempty[rb], ((rb_iter >> p.rb_shift) & 1) ^ 1, abort, p.status)) break;
           ++rb_iter;
-          mbar_arrive_expect_tx(&rbfull[rb], p.Rp * 4);
-          bulk_load(row_b_all + rb * rbf, p.negb + static_cast<size_t>(it.u) * p.Rp,
-                    p.Rp * 4, &rbfull[rb]);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&rbfull[rb], p.Rp * 4);
+            bulk_load(row_b_all + rb * rbf, p.negb + static_cast<size_t>(it.u) * p.Rp,
+                      p.Rp * 4, &rbfull[rb]);
+          }
         }
       }
 #pragma unroll
@@ -287,7 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (all lanes run the loop and wait converged; lane 0 issues MMAs and commits)
+    {
       const uint32_t a_base = smem_u32(a_buf), b_base = smem_u32(b_buf);
       int a_cnt[kTiles] = {0, 0};  // A loads consumed per tile slot
       int kt[kTiles] = {0, 0};     // accumulator fills per tile slot
@@ -297,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode<PASS>(p, item);
         for (int c = 0; ok && c < it.n_ch; ++c) {
           const int s = b_iter % NS;
-          if (!mbar_wait(&full[s], (b_iter / NS) & 1, abort, p.status)) {
+          if (!warp_wait(&full[s], (b_iter / NS) & 1, abort, p.status)) {
             ok = false;
             break;
           }
@@ -307,35 +316,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int t = 0; t < kTiles; ++t) {
             if (!ok || it.tile[t] < 0) continue;
             if (c == 0) {
-              if (!mbar_wait(&afull[t], a_cnt[t] & 1, abort, p.status)) {
+              if (!warp_wait(&afull[t], a_cnt[t] & 1, abort, p.status)) {
                 ok = false;
                 continue;
               }
               ++a_cnt[t];
             }
-            if (!mbar_wait(&accempty[t], (kt[t] & 1) ^ 1, abort, p.status)) {
+            if (!warp_wait(&accempty[t], (kt[t] & 1) ^ 1, abort, p.status)) {
               ok = false;
               continue;
             }
             tc_fence_after();
             const uint32_t a_tile = a_base + t * ly.a_bytes;
+            if (lane == 0) {
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const int kb = k / 4, kq = k % 4;
-              const uint64_t ad = sw128_desc(a_tile + kb * BM * 128 + kq * 32);
-              const uint64_t bd = sw128_desc(b_tile + kb * BN * 128 + kq * 32);
-              mma_bf16(tmem + t * BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+              for (int k = 0; k < D / 16; ++k) {
+                const int kb = k / 4, kq = k % 4;
+                const uint64_t ad = sw128_desc(a_tile + kb * BM * 128 + kq * 32);
+                const uint64_t bd = sw128_desc(b_tile + kb * BN * 128 + kq * 32);
+                mma_bf16(tmem + t * BN, ad, bd, idesc, k > 0 ? 1u : 0u);
+              }
+              mma_commit(&accfull[t]);
+              if (c == it.n_ch - 1) mma_commit(&aempty[t]);  // slot's A free for the next item
             }
-            mma_commit(&accfull[t]);
+            __syncwarp();
             ++kt[t];
-            if (c == it.n_ch - 1) mma_commit(&aempty[t]);  // slot's A free for the next item
           }
           if (!ok) break;
-          mma_commit(&empty[s]);
+          if (lane == 0) mma_commit(&empty[s]);
           ++b_iter;
         }
       }
-      mma_commit(done);
+      if (lane == 0) mma_commit(done);
+      __syncwarp();
       drain_wait(done, 0, p.status);
     }
     __syncwarp();
@@ -355,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tile = it.tile[t];
         if (!ok || tile < 0) continue;
         const int pb = (n_merge[t] & 1) * kTiles + t;
-        if (!epi_wait(&part_full[pb], (n_merge[t] >> 1) & 1, abort, p.status, lane)) {
+        if (!warp_wait(&part_full[pb], (n_merge[t] >> 1) & 1, abort, p.status)) {
           ok = false;
           continue;
         }
@@ -440,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_valid = tile >= 0 && (r < p.R) && (qpos >= it.pad) && (it.n_ch > 0);
         float mz = -INFINITY, sum = 0.f;  // max in raw logit units, sum rel. to it
         for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
-          if (!epi_wait(&accfull[wg], k & 1, abort, p.status, lane)) {
+          if (!warp_wait(&accfull[wg], k & 1, abort, p.status)) {
             ok = false;
             break;
           }
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tile < 0) continue;
         // partial (max, sum) of this half's columns of every chunk
         const int pb = (n_merge & 1) * kTiles + wg;
-        if (!epi_wait(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status, lane)) break;
+        if (!warp_wait(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status)) break;
         *reinterpret_cast<float2*>(part + ((pb * 2 + half) * BM + lrow) * 2) = make_float2(mz, sum);
         __syncwarp();
         if (lane == 0) mbar_arrive(&part_full[pb]);
@@ -493,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (it.n_ch == 0) continue;
         // the unit's negated row constants (bulk copy by the loader warp)
         const int rb = rb_iter & p.rb_shift;
-        if (!epi_wait(&rbfull[rb], (rb_iter >> p.rb_shift) & 1, abort, p.status, lane)) break;
+        if (!warp_wait(&rbfull[rb], (rb_iter >> p.rb_shift) & 1, abort, p.status)) break;
         ++rb_iter;
         const float* row_b = row_b_all + rb * rbf;
         const int pos = (tile >= 0 ? tile : 0) * BM + lrow;
@@ -502,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jmin = pos - (p.T - p.W);  // rows with j >= jmin see pos
         float2 acc = make_float2(0.f, 0.f);
         for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
-          if (!epi_wait(&accfull[wg], k & 1, abort, p.status, lane)) {
+          if (!warp_wait(&accfull[wg], k & 1, abort, p.status)) {
             ok = false;
             break;
           }
@@ -542,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tile < 0) continue;
         // partial usage over the query rows of this half's columns of every chunk
         const int pb = (n_merge & 1) * kTiles + wg;
-        if (!epi_wait(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status, lane)) break;
+        if (!warp_wait(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status)) break;
         part[(pb * 2 + half) * BM + lrow] = acc.x + acc.y;
         __syncwarp();
         if (lane == 0) mbar_arrive(&part_full[pb]);

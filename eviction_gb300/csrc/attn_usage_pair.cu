@@ -81,12 +81,12 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile i
                         : mbar_wait(bar, parity, abort, status);
 }
 
-// Warp-uniform wait of the epilogue and merge warps (lane 0 waits).
+// Warp-uniform wait of the epilogue and merge warps: all lanes wait converged
+// and vote on the outcome.
 __device__ __forceinline__ bool pwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                           uint32_t* status, int lane) {
-  int ok = 1;
-  if (lane == 0) ok = pwait<3>(bar, parity, abort, status) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+                                           uint32_t* status) {
+  const bool ok = pwait<3>(bar, parity, abort, status);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Per-item partials of the four groups handed to the merge warp, two buffers
@@ -382,7 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (PASS == 2 && it.n_ch == 0) continue;
       if (it.tile < 0) continue;
       const int pb = n_merge & 1;
-      if (!pwait_warp(&part_full[pb], (n_merge >> 1) & 1, abort, p.status, lane)) {
+      if (!pwait_warp(&part_full[pb], (n_merge >> 1) & 1, abort, p.status)) {
         ok = false;
         break;
       }
@@ -467,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // this group's chunks: ch with (f_base + ch) % 4 == grp
         for (int ch = (grp - f_base % kGroups + kGroups) % kGroups; ch < it.n_ch; ch += kGroups) {
           const int kf = (f_base + ch) / kGroups;  // fill count of this accumulator
-          if (!pwait_warp(&accfull[grp], kf & 1, abort, p.status, lane)) {
+          if (!pwait_warp(&accfull[grp], kf & 1, abort, p.status)) {
             ok = false;
             break;
           }
@@ -509,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (tile < 0) continue;
         const int pb = n_merge & 1;
-        if (!pwait_warp(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status, lane)) break;
+        if (!pwait_warp(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status)) break;
         *reinterpret_cast<float2*>(part + ((pb * kGroups + grp) * BM + lrow) * 2) =
             make_float2(mz, sum);
         __syncwarp();
@@ -518,7 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       } else {
         if (it.n_ch == 0) continue;
         const int rb = rb_iter & p.rb_shift;
-        if (!pwait_warp(&rbfull[rb], (rb_iter >> p.rb_shift) & 1, abort, p.status, lane)) break;
+        if (!pwait_warp(&rbfull[rb], (rb_iter >> p.rb_shift) & 1, abort, p.status)) break;
         ++rb_iter;
         const float* row_b = row_b_all + rb * rbf;
         const int pos = (tile >= 0 ? tile : 0) * BM + lrow;
@@ -528,7 +528,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float2 acc = make_float2(0.f, 0.f);
         for (int ch = (grp - f_base % kGroups + kGroups) % kGroups; ch < it.n_ch; ch += kGroups) {
           const int kf = (f_base + ch) / kGroups;
-          if (!pwait_warp(&accfull[grp], kf & 1, abort, p.status, lane)) {
+          if (!pwait_warp(&accfull[grp], kf & 1, abort, p.status)) {
             ok = false;
             break;
           }
@@ -569,7 +569,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (tile < 0) continue;
         const int pb = n_merge & 1;
-        if (!pwait_warp(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status, lane)) break;
+        if (!pwait_warp(&part_empty[pb], ((n_merge >> 1) & 1) ^ 1, abort, p.status)) break;
         part[(pb * kGroups + grp) * BM + lrow] = acc.x + acc.y;
         __syncwarp();
         if (lane == 0) mbar_arrive(&part_full[pb]);
