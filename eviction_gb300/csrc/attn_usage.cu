@@ -481,13 +481,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             release();
             row_pair(v, bmx, c, mz, sum);
           } else {
-            // masked or partial chunk: one block at a time
+            // masked or partial chunk, one 32-column block at a time: a block
+            // that no row of the warp sees is skipped, one that every row sees
+            // in full takes the unmasked arithmetic
             for (int b = 0; b < nb; ++b) {
+              const int pb0 = p0 + 32 * b;
+              const bool all = __all_sync(0xffffffffu, lo <= pb0 && hi >= pb0 + 31);
+              const bool some = __any_sync(0xffffffffu, min(hi, pb0 + 31) >= max(lo, pb0));
               __syncwarp();
-              tmem_ld32(t_lane + 32 * b, v[0]);
-              tmem_ld_wait();
-              if (b == nb - 1) release();
-              row_block<false>(v[0], -INFINITY, p0 + 32 * b, lo, hi, c, mz, sum);
+              if (all) {
+                tmem_ld32_max(t_lane + 32 * b, v[0], bmx[0]);
+                tmem_ld_wait();
+                if (b == nb - 1) release();
+                row_block<true>(v[0], bmx[0], pb0, lo, hi, c, mz, sum);
+              } else if (some) {
+                tmem_ld32(t_lane + 32 * b, v[0]);
+                tmem_ld_wait();
+                if (b == nb - 1) release();
+                row_block<false>(v[0], -INFINITY, pb0, lo, hi, c, mz, sum);
+              } else if (b == nb - 1) {
+                release();
+              }
             }
             if (nb == 0) release();
           }
@@ -537,12 +551,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             release();
             slot_pair(v, row_b + r0 + 64, c, acc);
           } else {
+            // one 32-row block at a time; with windows of whole blocks, a block
+            // of rows that no slot of the warp is seen by is skipped and one
+            // whose rows see every slot takes the unmasked arithmetic
             for (int b = 0; b < nb; ++b) {
+              const int rb0 = r0 + 32 * b;
+              bool all = false, some = true;
+              if (p.W % 32 == 0) {
+                const int j0 = rb0 % p.W;  // the block's window indices j0 .. j0+31
+                all = __all_sync(0xffffffffu, j0 >= jmin);
+                some = __any_sync(0xffffffffu, j0 + 31 >= jmin);
+              }
               __syncwarp();
-              tmem_ld32(t_lane + 32 * b, v[0]);
-              tmem_ld_wait();
-              if (b == nb - 1) release();
-              slot_block<false>(v[0], row_b + r0 + 32 * b, r0 + 32 * b, p.W, jmin, c, acc);
+              if (all) {
+                tmem_ld32(t_lane + 32 * b, v[0]);
+                tmem_ld_wait();
+                if (b == nb - 1) release();
+                slot_block<true>(v[0], row_b + rb0, rb0, p.W, jmin, c, acc);
+              } else if (some) {
+                tmem_ld32(t_lane + 32 * b, v[0]);
+                tmem_ld_wait();
+                if (b == nb - 1) release();
+                slot_block<false>(v[0], row_b + rb0, rb0, p.W, jmin, c, acc);
+              } else if (b == nb - 1) {
+                release();
+              }
             }
             if (nb == 0) release();
           }
