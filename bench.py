@@ -44,9 +44,10 @@ KERNEL_SOURCES = {
     "refresh_trigger": "refresh.cu",
     "usage_pass1_rowstats_tcgen05": ("attn_usage.cu", "attn_common.cuh"),
     "usage_pass2_colsum_tcgen05": ("attn_usage.cu", "attn_common.cuh"),
-    "mass_pool_ema": "mass_post.cu",
-    "segment_quota": "segment_quota.cu",
-    "select_topk": "select.cu",
+    "mass_pool_ema": ("mass_post.cu", "unit_phases.cuh"),
+    "segment_quota": ("segment_quota.cu", "unit_phases.cuh"),
+    "select_topk": ("select.cu", "unit_phases.cuh"),
+    "mass_segment_select": ("unit_post.cu", "unit_phases.cuh"),
     "gather_compact": "compact.cu",
     "redundancy_score": "redundancy.cu",
 }
@@ -126,6 +127,9 @@ def unit_work(w, T_valid, T):
         "mass_pool_ema": ("hbm", 0.0, 4.0 * T * 5 + 8.0 * G * W),
         "segment_quota": ("hbm", 0.0, 4.0 * T),
         "select_topk": ("hbm", 0.0, 4.0 * T + 4.0 * Kb),
+        # the three above in one launch: mass's traffic and the kept indices
+        # (the mass and the score stay on chip for the later steps)
+        "mass_segment_select": ("hbm", 0.0, 4.0 * T * 5 + 8.0 * G * W + 4.0 * Kb),
         # kept K and V rows read, written; credit read/written; indices read
         "gather_compact": ("hbm", 0.0, 8.0 * Kb * d + 12.0 * Kb),
         # the same rows and credit moved into pool blocks; plus indices validated
@@ -548,12 +552,10 @@ def run_ours(args, w):
             table.copy_(table0)
             free.copy_(free0)
             top.copy_(top0)
-            h.mass(inp.q, inp.k, T, inp.pad, inp.n_carry, inp.credit, stage["credit_post"],
-                   stage["mass"], stage["score"])
-            h.segment_quota(stage["mass"], T, inp.pad, stage["seg_start"], stage["seg_len"],
-                            stage["quota"], stage["n_seg"])
-            h.select(stage["score"], T, inp.pad, stage["seg_start"], stage["seg_len"],
-                     stage["quota"], stage["n_seg"], out["kept_idx"], out["n_kept"])
+            h.mass_select(inp.q, inp.k, T, inp.pad, inp.n_carry, inp.credit,
+                          stage["credit_post"], stage["mass"], stage["score"],
+                          stage["seg_start"], stage["seg_len"], stage["quota"], stage["n_seg"],
+                          out["kept_idx"], out["n_kept"])
             h.compact_paged(k_pool, v_pool, bs, seq_len, inp.pad, out["kept_idx"], out["n_kept"],
                             stage["credit_post"], T, out["credit_out"], table, table_new, free,
                             top)

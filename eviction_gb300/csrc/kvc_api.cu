@@ -45,7 +45,7 @@ int cuda_fail(kvc_handle* h, cudaError_t e, const char* where) {
 const char* const kKernelNames[kvc::kNumKernels] = {
     "usage_pass1_rowstats_tcgen05", "usage_pass2_colsum_tcgen05", "mass_pool_ema",
     "segment_quota", "select_topk", "gather_compact", "refresh_trigger", "compact_paged",
-    "redundancy_score"};
+    "redundancy_score", "mass_segment_select"};
 
 cudaEvent_t prof_event(kvc_handle* h) {
   auto& P = h->prof;
@@ -93,9 +93,9 @@ float scale_log2_of(const kvc_config& c) {
   return static_cast<float>(s * 1.4426950408889634);
 }
 
-int run_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T, const int32_t* pad,
-             const int32_t* n_carry, const float* credit_in, float* credit_post, float* mass,
-             float* score, cudaStream_t s) {
+// Step 1: both passes of the window attention usage into the workspace.
+int run_usage(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T, const int32_t* pad,
+              cudaStream_t s) {
   kvc::UsageArgs a{q, k, pad, T, scale_log2_of(h->cfg)};
   std::string err;
   for (int pass = 1; pass <= 2; ++pass) {
@@ -107,6 +107,14 @@ int run_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T, const i
       return err.empty() ? cuda_fail(h, e, "attention usage") : fail(h, KVC_ERR_CUDA, err);
     mark_end(h, pass == 1 ? kvc::kKernelUsagePass1 : kvc::kKernelUsagePass2, b, s);
   }
+  return KVC_OK;
+}
+
+int run_mass(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T, const int32_t* pad,
+             const int32_t* n_carry, const float* credit_in, float* credit_post, float* mass,
+             float* score, cudaStream_t s) {
+  int rc = run_usage(h, q, k, T, pad, s);
+  if (rc) return rc;
   cudaEvent_t b = mark_begin(h, s);
   cudaError_t e =
       kvc::launch_mass_post(h, T, pad, n_carry, credit_in, credit_post, mass, score, s);
@@ -157,22 +165,47 @@ int run_compact(kvc_handle* h, const uint16_t* k, const uint16_t* v, const float
   return KVC_OK;
 }
 
+// Steps 1-4 on validated pointers: usage, mass and credit, segments and
+// quotas, kept indices.  Units of up to 4096 slots run mass, segmentation and
+// selection as one fused launch (same bits as the three stand-alone kernels);
+// the redundancy mix sits between segmentation and selection, so with it on,
+// and for longer units, the stand-alone kernels run.
+int run_mass_select(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T,
+                    const int32_t* pad, const int32_t* n_carry, const float* credit_in,
+                    float* credit_post, float* mass, float* score, int32_t* seg_start,
+                    int32_t* seg_len, int32_t* quota, int32_t* n_seg, int32_t* kept_idx,
+                    int32_t* n_kept, cudaStream_t s) {
+  const size_t fused_smem = kvc::unit_post_smem_bytes(h->cfg, T);
+  if (!(h->cfg.redundancy_sigma > 0.f) && fused_smem > 0 && fused_smem <= h->smem_optin) {
+    int rc = run_usage(h, q, k, T, pad, s);
+    if (rc) return rc;
+    cudaEvent_t b = mark_begin(h, s);
+    cudaError_t e = kvc::launch_unit_post(h, T, pad, n_carry, credit_in, credit_post, mass,
+                                          score, seg_start, seg_len, quota, n_seg, kept_idx,
+                                          n_kept, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "mass/segment/select");
+    mark_end(h, kvc::kKernelUnitPost, b, s);
+    return KVC_OK;
+  }
+  int rc = run_mass(h, q, k, T, pad, n_carry, credit_in, credit_post, mass, score, s);
+  if (rc) return rc;
+  rc = run_segment_quota(h, mass, T, pad, seg_start, seg_len, quota, n_seg, s);
+  if (rc) return rc;
+  if (h->cfg.redundancy_sigma > 0.f) {  // the selection score, in place
+    rc = run_redundancy(h, k, score, T, pad, score, nullptr, s);
+    if (rc) return rc;
+  }
+  return run_select(h, score, T, pad, seg_start, seg_len, quota, n_seg, kept_idx, n_kept, s);
+}
+
 // Steps 1-6 on validated pointers, intermediates in the workspace.
 int run_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_t* v, int T,
               const int32_t* pad, const int32_t* n_carry, const float* credit_in,
               uint16_t* k_out, uint16_t* v_out, float* credit_out, int32_t* kept_idx,
               int32_t* n_kept, cudaStream_t s) {
   const kvc::Workspace& w = h->ws;
-  int rc = run_mass(h, q, k, T, pad, n_carry, credit_in, w.credit_post, w.mass, w.score, s);
-  if (rc) return rc;
-  rc = run_segment_quota(h, w.mass, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, s);
-  if (rc) return rc;
-  if (h->cfg.redundancy_sigma > 0.f) {  // the selection score, in place
-    rc = run_redundancy(h, k, w.score, T, pad, w.score, nullptr, s);
-    if (rc) return rc;
-  }
-  rc = run_select(h, w.score, T, pad, w.seg_start, w.seg_len, w.quota, w.n_seg, kept_idx,
-                  n_kept, s);
+  int rc = run_mass_select(h, q, k, T, pad, n_carry, credit_in, w.credit_post, w.mass, w.score,
+                           w.seg_start, w.seg_len, w.quota, w.n_seg, kept_idx, n_kept, s);
   if (rc) return rc;
   return run_compact(h, k, v, w.credit_post, T, kept_idx, n_kept, k_out, v_out, credit_out, s);
 }
@@ -339,6 +372,7 @@ int kvc_create(const kvc_config* cfg, kvc_handle** out) {
   h->cfg = *cfg;
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
+  h->smem_optin = prop.sharedMemPerBlockOptin;
   kvc::Dims& d = h->dims;
   d.L = cfg->n_layers;
   d.B = cfg->batch;
@@ -587,6 +621,33 @@ int kvc_refresh_decision(kvc_handle* h, const uint16_t* q, float* q_ref, float t
   if (e != cudaSuccess) return cuda_fail(h, e, "refresh trigger");
   mark_end(h, kvc::kKernelRefresh, b, s);
   return KVC_OK;
+}
+
+int kvc_mass_select(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T,
+                    const int32_t* pad, const int32_t* n_carry, const float* credit_in,
+                    float* credit_post, float* mass, float* score, int32_t* seg_start,
+                    int32_t* seg_len, int32_t* quota, int32_t* n_seg, int32_t* kept_idx,
+                    int32_t* n_kept, void* stream) {
+  if (!h) return KVC_ERR_ARG;
+  int rc = check_T(h, T);
+  if (rc) return rc;
+  KVC_REQUIRE_PTR(q);
+  KVC_REQUIRE_PTR(k);
+  KVC_REQUIRE_PTR(pad);
+  KVC_REQUIRE_PTR(n_carry);
+  KVC_REQUIRE_PTR(credit_in);
+  KVC_REQUIRE_PTR(credit_post);
+  KVC_REQUIRE_PTR(mass);
+  KVC_REQUIRE_PTR(score);
+  KVC_REQUIRE_PTR(seg_start);
+  KVC_REQUIRE_PTR(seg_len);
+  KVC_REQUIRE_PTR(quota);
+  KVC_REQUIRE_PTR(n_seg);
+  KVC_REQUIRE_PTR(kept_idx);
+  KVC_REQUIRE_PTR(n_kept);
+  return run_mass_select(h, q, k, T, pad, n_carry, credit_in, credit_post, mass, score,
+                         seg_start, seg_len, quota, n_seg, kept_idx, n_kept,
+                         static_cast<cudaStream_t>(stream));
 }
 
 int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k, const uint16_t* v,

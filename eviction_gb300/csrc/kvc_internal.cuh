@@ -52,6 +52,7 @@ enum KernelId {
   kKernelRefresh,
   kKernelCompactPaged,
   kKernelRedundancy,
+  kKernelUnitPost,
   kNumKernels
 };
 
@@ -88,6 +89,7 @@ struct kvc_handle {
   kvc::Workspace ws;
   int device = 0;
   int num_sms = 0;
+  size_t smem_optin = 0;  // shared memory a block may opt in to
   std::string last_error;
   kvc::Profiler prof;
   kvc::HostIO io;
@@ -129,6 +131,18 @@ cudaError_t launch_select(const kvc_handle* h, const float* score, int T,
                           const int32_t* seg_len, const int32_t* quota,
                           const int32_t* n_seg, int32_t* kept_idx,
                           int32_t* n_kept, cudaStream_t s);
+
+// Mass, segmentation with quotas and selection fused in one launch (one CTA
+// per unit, unit_post.cu); for units of up to 4096 slots.  Same outputs, bit
+// for bit, as launch_mass_post + launch_segment_quota + launch_select.
+cudaError_t launch_unit_post(const kvc_handle* h, int T, const int32_t* pad,
+                             const int32_t* n_carry, const float* credit_in,
+                             float* credit_post, float* mass, float* score, int32_t* seg_start,
+                             int32_t* seg_len, int32_t* quota, int32_t* n_seg,
+                             int32_t* kept_idx, int32_t* n_kept, cudaStream_t s);
+
+// Shared memory of the fused kernel for units of T slots (0: T too long for it).
+size_t unit_post_smem_bytes(const kvc_config& c, int T);
 
 // Host validation of a configuration (every field, and the unit and row counts
 // in 64-bit arithmetic); KVC_OK or a negative code with the reason in *why.

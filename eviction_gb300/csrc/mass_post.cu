@@ -12,6 +12,12 @@
 // The base score ("RefreshKV: ...", A2: max pooling of neighbouring attention
 // scores; A6: kernel 7) is the filled usage max-pooled over valid neighbours.
 //
+// Reading of the normalisations: m sums to one, so the credit total is
+// 1 + lambda * (sum over carried slots of (c_in - m)), and the mix
+// beta*m + (1-beta)*c/sum(c) already sums to one; one block reduction of three
+// totals (all of m, the carried slots' c_in and m) gives every value, and the
+// last normalize() is a division by one, left out.
+//
 // Units up to 4096 slots take one pass with the filled usage in shared memory
 // and per-slot values in registers; longer ones sweep global memory (the
 // unit's data stays in L1/L2 between sweeps).  Every sum is a strided
@@ -19,65 +25,14 @@
 // identical bits.
 #include <cmath>
 
-#include "kvc_internal.cuh"
+#include "unit_phases.cuh"
 
 namespace kvc {
 int attention_row_stride(int R);
 namespace {
 
-constexpr int kThreads = 256;
-
-template <int NT = kThreads>
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  __syncthreads();  // red may still be read by a previous reduction
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-  if (threadIdx.x < 32) {
-    t = (lane < NT / 32) ? red[lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (lane == 0) red[NT / 32] = t;
-  }
-  __syncthreads();
-  return red[NT / 32];
-}
-
-template <int NT = kThreads>
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float t = (lane < NT / 32) ? red[lane] : -INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, o));
-    if (lane == 0) red[NT / 32] = t;
-  }
-  __syncthreads();
-  return red[NT / 32];
-}
-
-struct PostParams {
-  int T, R, W, G, B, H;
-  int avg_pool, max_pool;
-  float eps, lambda, beta;
-  int Rp;
-  const float* pmax;  // [U][Rp] largest probability of each row (0 if absent)
-  float* usage;       // [U][T] raw usage, filled in place
-  const int32_t* pad;
-  const int32_t* n_carry;
-  const float* credit_in;
-  float* credit_post;
-  float* mass;
-  float* score;
-};
+using unit::PostParams;
+using unit::block_max;
 
 // Units longer than kSmemT slots sweep global memory.  They are few (a long
 // cache holds few sequences), so each takes a CTA of NT = 1024 threads: four
@@ -85,7 +40,7 @@ struct PostParams {
 template <int NT>
 __global__ void __launch_bounds__(NT)
     mass_post_kernel(PostParams p) {
-  __shared__ float red[NT / 32 + 1];
+  __shared__ float red[3 * (NT / 32 + 1)];
   const int u = blockIdx.x;
   const int b = (u / p.H) % p.B;
   const int T = p.T;
@@ -120,10 +75,12 @@ __global__ void __launch_bounds__(NT)
   }
   __syncthreads();
 
-  // score = max-pooled usage; first mass total
+  // score = max-pooled usage; the mass totals (as in unit::mass_phase: one
+  // reduction of the up total and the carried slots' credit-in and up)
+  const int n_carry = min(max(p.n_carry[b], 0), T - pad);
   const int ra = p.avg_pool / 2, rm = p.max_pool / 2;
   const float inv_k = 1.0f / static_cast<float>(p.avg_pool);
-  float tot = 0.f;
+  float tot = 0.f, cin_c = 0.f, up_c = 0.f;
   for (int i = threadIdx.x; i < T; i += NT) {
     if (i < pad) {
       score[i] = -INFINITY;
@@ -134,167 +91,47 @@ __global__ void __launch_bounds__(NT)
     score[i] = mx;
     float s = 0.f;
     for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
-    tot += fmaxf(s * inv_k, 0.f) + p.eps;
-  }
-  const float total1 = block_sum<NT>(tot, red);
-
-  // mass and credit
-  const int n_carry = min(max(p.n_carry[b], 0), T - pad);
-  const float lam = p.lambda;
-  float ctot = 0.f;
-  for (int i = threadIdx.x; i < T; i += NT) {
-    if (i < pad) {
-      mass[i] = 0.f;
-      cpost[i] = 0.f;
-      continue;
+    const float up = fmaxf(s * inv_k, 0.f) + p.eps;
+    tot += up;
+    if (i < pad + n_carry) {
+      cin_c += cin[i];
+      up_c += up;
     }
-    float s = 0.f;
-    for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
-    const float m = (fmaxf(s * inv_k, 0.f) + p.eps) / total1;
-    const float prior = (i < pad + n_carry) ? cin[i] : m;
-    const float c = lam * prior + (1.0f - lam) * m;
-    mass[i] = m;
-    cpost[i] = c;
-    ctot += c;
   }
-  const float c_total = block_sum<NT>(ctot, red);
+  const float3 tt = unit::block_sum3<NT>(make_float3(tot, cin_c, up_c), red);
+  const float total1 = tt.x;
+  const float lam = p.lambda, beta = p.beta;
+  const float c_total = 1.0f + lam * (tt.y - tt.z / total1);
 
-  // mix and normalise
-  const float beta = p.beta;
-  float mtot = 0.f;
-  for (int i = pad + threadIdx.x; i < T; i += NT) {
-    const float m = mass[i];
-    const float cn = (c_total > 0.f) ? cpost[i] / c_total : m;
-    const float mix = beta * m + (1.0f - beta) * cn;
-    mass[i] = mix;
-    mtot += mix;
+  // mass (m_used) and credit
+  for (int i = threadIdx.x; i < T; i += NT) {
+    float mu = 0.f, c = 0.f;
+    if (i >= pad) {
+      float s = 0.f;
+      for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
+      const float m = (fmaxf(s * inv_k, 0.f) + p.eps) / total1;
+      c = (i < pad + n_carry) ? lam * cin[i] + (1.0f - lam) * m : m;
+      const float cn = (c_total > 0.f) ? c / c_total : m;
+      mu = beta * m + (1.0f - beta) * cn;
+    }
+    mass[i] = mu;
+    cpost[i] = c;
   }
-  const float mix_total = block_sum<NT>(mtot, red);
-  for (int i = pad + threadIdx.x; i < T; i += NT) mass[i] = mass[i] / mix_total;
 }
 
-// Units of up to kSmemT slots: one pass.  The filled usage of the unit sits in
-// shared memory (the pooling windows read it there), each thread keeps its
-// slots' values in registers across the normalisations, and score, mass and
-// credit are written once.  The arithmetic and the summation order (per thread
-// over its slots, then block_sum) are those of the general kernel below.
-constexpr int kSmemT = 4096;
-
+// Units of up to kSmemT slots: one pass (unit::mass_phase; the fused per-unit
+// kernel runs the same function with the same CTA shape, unit::mass_shape).
+// The filled usage of the unit sits in shared memory (the pooling windows read
+// it there), each thread keeps its slots' values in registers across the
+// three totals, and score, mass and credit are written once.
 // Latency-bound: one CTA per unit, so the more CTAs an SM holds the better.
-// Up to 8 slots per thread the kernel fits in 32 registers without spilling,
-// which lets 8 CTAs share an SM (5 at its natural 47 registers).
-template <int kEpt>  // slots per thread: T <= kEpt * kThreads
-__global__ void __launch_bounds__(kThreads, kEpt <= 8 ? 8 : 4)
+// Up to 6 slots per thread it fits in 32 registers, eight CTAs per SM.
+template <int NT, int kEpt>  // T <= kEpt * NT
+__global__ void __launch_bounds__(NT, kEpt <= 6 ? 8 : (kEpt <= 8 ? 6 : 4))
     mass_post_smem_kernel(PostParams p) {
-  __shared__ float red[kThreads / 32 + 1];
-  __shared__ float a[kEpt * kThreads];
-  const int u = blockIdx.x;
-  const int b = (u / p.H) % p.B;
-  const int T = p.T;
-  const int pad = min(max(p.pad[b], 0), T);
-  const size_t base = static_cast<size_t>(u) * T;
-  float* mass = p.mass + base;
-  float* score = p.score + base;
-  float* cpost = p.credit_post + base;
-  const float* cin = p.credit_in + base;
-  const float* usage = p.usage + base;
-
-  if (pad >= T) {
-    for (int i = threadIdx.x; i < T; i += kThreads) {
-      mass[i] = 0.f;
-      score[i] = -INFINITY;
-      cpost[i] = 0.f;
-    }
-    return;
-  }
-  const int n_carry = min(max(p.n_carry[b], 0), T - pad);
-  // this thread's credit-in values, loaded early (used after two reductions)
-  float cprior[kEpt];
-#pragma unroll
-  for (int k = 0; k < kEpt; ++k) {
-    const int i = threadIdx.x + k * kThreads;
-    cprior[k] = (i >= pad && i < pad + n_carry) ? cin[i] : 0.f;
-  }
-
-  float pm = 0.f;
-  for (int r = threadIdx.x; r < p.R; r += kThreads)
-    pm = fmaxf(pm, p.pmax[static_cast<size_t>(u) * p.Rp + r]);
-  const float fill = block_max(pm, red);
-
-  const int j_lo = max(0, pad - (T - p.W));
-#pragma unroll
-  for (int k = 0; k < kEpt; ++k) {
-    const int i = threadIdx.x + k * kThreads;
-    if (i < T) {
-      const int unseen = max(0, min(p.W, i - T + p.W) - j_lo) * p.G;
-      a[i] = i >= pad ? usage[i] + fill * static_cast<float>(unseen) : 0.f;
-    }
-  }
-  __syncthreads();
-
-  const int ra = p.avg_pool / 2, rm = p.max_pool / 2;
-  const float inv_k = 1.0f / static_cast<float>(p.avg_pool);
-  float up[kEpt];  // max(avg pool, 0) + eps
-  float tot = 0.f;
-#pragma unroll
-  for (int k = 0; k < kEpt; ++k) {
-    const int i = threadIdx.x + k * kThreads;
-    up[k] = 0.f;
-    if (i >= T) continue;
-    if (i < pad) {
-      score[i] = -INFINITY;
-      continue;
-    }
-    float mx = -INFINITY;
-    for (int t = max(pad, i - rm); t <= min(T - 1, i + rm); ++t) mx = fmaxf(mx, a[t]);
-    score[i] = mx;
-    float sm = 0.f;
-    for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) sm += a[t];
-    up[k] = fmaxf(sm * inv_k, 0.f) + p.eps;
-    tot += up[k];
-  }
-  const float total1 = block_sum(tot, red);
-
-  const float lam = p.lambda;
-  float ctot = 0.f;
-#pragma unroll
-  for (int k = 0; k < kEpt; ++k) {
-    const int i = threadIdx.x + k * kThreads;
-    if (i < pad || i >= T) continue;
-    const float m = up[k] / total1;
-    const float prior = (i < pad + n_carry) ? cprior[k] : m;
-    const float c = lam * prior + (1.0f - lam) * m;
-    up[k] = m;
-    cprior[k] = c;
-    ctot += c;
-  }
-  const float c_total = block_sum(ctot, red);
-
-  const float beta = p.beta;
-  float mtot = 0.f;
-#pragma unroll
-  for (int k = 0; k < kEpt; ++k) {
-    const int i = threadIdx.x + k * kThreads;
-    if (i < pad || i >= T) continue;
-    const float m = up[k];
-    const float cn = (c_total > 0.f) ? cprior[k] / c_total : m;
-    const float mix = beta * m + (1.0f - beta) * cn;
-    up[k] = mix;
-    mtot += mix;
-  }
-  const float mix_total = block_sum(mtot, red);
-#pragma unroll
-  for (int k = 0; k < kEpt; ++k) {
-    const int i = threadIdx.x + k * kThreads;
-    if (i >= T) continue;
-    if (i < pad) {
-      mass[i] = 0.f;
-      cpost[i] = 0.f;
-    } else {
-      mass[i] = up[k] / mix_total;
-      cpost[i] = cprior[k];
-    }
-  }
+  __shared__ float red[3 * (NT / 32 + 1)];
+  __shared__ float a[kEpt * NT];
+  unit::mass_phase<kEpt, NT>(p, blockIdx.x, a, red, nullptr, nullptr);
 }
 
 }  // namespace
@@ -325,14 +162,17 @@ cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
   p.credit_post = credit_post;
   p.mass = mass;
   p.score = score;
-  if (T <= 4 * kThreads)
-    mass_post_smem_kernel<4><<<dm.U, kThreads, 0, s>>>(p);
-  else if (T <= 8 * kThreads)
-    mass_post_smem_kernel<8><<<dm.U, kThreads, 0, s>>>(p);
-  else if (T <= kSmemT)
-    mass_post_smem_kernel<kSmemT / kThreads><<<dm.U, kThreads, 0, s>>>(p);
-  else
+  if (T <= unit::kSmemT) {
+    int nt, ept;
+    unit::mass_shape(T, &nt, &ept);
+    auto k = ept == 4 ? mass_post_smem_kernel<256, 4>
+             : ept == 6 ? mass_post_smem_kernel<256, 6>
+             : ept == 8 ? mass_post_smem_kernel<256, 8>
+                        : mass_post_smem_kernel<256, 16>;
+    k<<<dm.U, nt, 0, s>>>(p);
+  } else {
     mass_post_kernel<1024><<<dm.U, 1024, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

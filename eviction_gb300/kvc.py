@@ -21,7 +21,7 @@ ENTRY_POINTS = ("kvc_default_config", "kvc_create", "kvc_destroy", "kvc_stage_si
                 "kvc_get_device_status", "kvc_last_error", "kvc_status_string", "kvc_profile",
                 "kvc_profile_read", "kvc_mass_noalloc", "kvc_refresh_decision",
                 "kvc_compact_paged", "kvc_redundancy_score", "kvc_wait_self_test",
-                "kvc_event_host")
+                "kvc_event_host", "kvc_mass_select")
 
 STATUS = {0: "KVC_OK", -1: "KVC_ERR_ARG", -2: "KVC_ERR_SHAPE", -3: "KVC_ERR_ALIGN",
           -4: "KVC_ERR_NOMEM", -5: "KVC_ERR_CUDA", -6: "KVC_ERR_DEVICE", -7: "KVC_ERR_TIMEOUT",
@@ -146,6 +146,7 @@ def load_library():
     L.kvc_select.argtypes = [_P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P]
     L.kvc_compact.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]
     L.kvc_event.argtypes = [_P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+    L.kvc_mass_select.argtypes = [_P, _P, _P, _I] + [_P] * 13
     L.kvc_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32), _P]
     L.kvc_last_error.argtypes = [_P]
     L.kvc_last_error.restype = ctypes.c_char_p
@@ -280,6 +281,22 @@ class Handle:
             _dev(k_out, torch.bfloat16, "k_out"), _dev(v_out, torch.bfloat16, "v_out"),
             _dev(credit_out, torch.float32, "credit_out"), _stream_ptr(stream))
         self._check(rc, "kvc_compact")
+
+    def mass_select(self, q, k, T, pad, n_carry, credit_in, credit_post, mass, score,
+                    seg_start, seg_len, quota, n_seg, kept_idx, n_kept, stream=None):
+        """kvc_mass_select: steps 1-5 (kvc_mass, kvc_segment_quota, kvc_select
+        chained) with every intermediate in the given buffers."""
+        import torch
+        rc = load_library().kvc_mass_select(
+            self._h, _dev(q, torch.bfloat16, "q"), _dev(k, torch.bfloat16, "k"), T,
+            _dev(pad, torch.int32, "pad"), _dev(n_carry, torch.int32, "n_carry"),
+            _dev(credit_in, torch.float32, "credit_in"),
+            _dev(credit_post, torch.float32, "credit_post"), _dev(mass, torch.float32, "mass"),
+            _dev(score, torch.float32, "score"), _dev(seg_start, torch.int32, "seg_start"),
+            _dev(seg_len, torch.int32, "seg_len"), _dev(quota, torch.int32, "quota"),
+            _dev(n_seg, torch.int32, "n_seg"), _dev(kept_idx, torch.int32, "kept_idx"),
+            _dev(n_kept, torch.int32, "n_kept"), _stream_ptr(stream))
+        self._check(rc, "kvc_mass_select")
 
     def event(self, q, k, v, T, pad, n_carry, credit_in, k_out, v_out, credit_out, kept_idx,
               n_kept, stream=None):

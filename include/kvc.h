@@ -240,11 +240,36 @@ int kvc_redundancy_score(kvc_handle* h, const uint16_t* k, const float* score, i
                          const int32_t* pad, float* sel_score, float* redundancy,
                          void* stream);
 
+/* Steps 1-5 in one call: kvc_mass, kvc_segment_quota and kvc_select chained,
+ * with every intermediate written to the caller's buffers.
+ * Defined by AMS, Method, Key designs 1-4 up to the kept set (usage and mass,
+ * cut points, quotas and must-keep, in-segment selection), with the RefreshKV
+ * A2/A6 score, and by the overhead statement of the same section (mass
+ * processing and the prefix sum are O(H_kv T) work after the attention).  For
+ * T <= 4096 the mass, segmentation and selection run as one launch (one CTA
+ * per unit, mass, score and segments held in shared memory between the
+ * steps); every output is bit-identical to the three stage calls.  With
+ * cfg.redundancy_sigma > 0, or longer units, the stage kernels run in turn and
+ * score is overwritten by kvc_redundancy_score's mix before the selection.
+ * For callers that compact on their own (kvc_compact_paged).
+ *   q, k, pad, n_carry, credit_in, credit_post, mass, score  as for kvc_mass;
+ *   seg_start, seg_len, quota, n_seg  as kvc_segment_quota writes them;
+ *   kept_idx, n_kept  as kvc_select writes them.
+ * Device pointers, caller-owned, 16-byte aligned; asynchronous on `stream`;
+ * the errors of kvc_mass. */
+int kvc_mass_select(kvc_handle* h, const uint16_t* q, const uint16_t* k, int T,
+                    const int32_t* pad, const int32_t* n_carry,
+                    const float* credit_in, float* credit_post, float* mass,
+                    float* score, int32_t* seg_start, int32_t* seg_len,
+                    int32_t* quota, int32_t* n_seg, int32_t* kept_idx,
+                    int32_t* n_kept, void* stream);
+
 /* The whole event, steps 1-6, with the intermediates in the workspace.
  * Defined by AMS, Method, Key designs 1-4 in order (usage and mass, cut points,
  * quotas and must-keep, in-segment selection and physical compaction), with the
- * RefreshKV A2/A6 score, exactly as the stage entry points above chain them;
- * the arguments are those of kvc_mass and kvc_compact.  With
+ * RefreshKV A2/A6 score: kvc_mass_select, then kvc_compact, with the same
+ * bits as the stage entry points chained; the arguments are those of kvc_mass
+ * and kvc_compact.  With
  * cfg.redundancy_sigma > 0, step 5 selects on kvc_redundancy_score's mix. */
 int kvc_event(kvc_handle* h, const uint16_t* q, const uint16_t* k,
               const uint16_t* v, int T, const int32_t* pad,

@@ -38,4 +38,7 @@ def test_bench_line_keeps_the_contract():
     assert e2e["value"] != line["value"]  # measured through host buffers, not a copy
     clocks = line["clocks"]
     assert "sm_mhz" in clocks and "sm_max_mhz" in clocks and "reasons" in clocks
-    assert line["gpu_launches"] == 6 * 2  # six kernels per event, two timed events
+    # two attention passes, the fused mass/segment/select kernel and the gather
+    # per event (units of 1536 slots), two timed events
+    assert line["gpu_launches"] == 4 * 2
+    assert sum(k["launches"] for k in line["kernels"]) == line["gpu_launches"]

@@ -13,6 +13,8 @@ Bars (floating point from the benchmark spec's tolerance, integers bit-exact):
 Sizes: several 128-row / 128-slot tiles with a ragged tail, left padding, a
 sequence shorter than the window, an all-padding sequence, d = 64 and 128.
 """
+import zlib
+
 import numpy as np
 import pytest
 import torch
@@ -125,6 +127,52 @@ def test_segment_quota_random_masses(ref, seed, T, budget, delta, seg_min, seg_m
     h = kvc.Handle(cfg)
     st, ln, qu, ns = gu.gpu_segment_quota(h, mass, pads, T)
     p = ref.RefParams(group=1, head_dim=64, window=8, budget=budget, delta=delta,
+                      seg_min=seg_min, seg_max=seg_max)
+    rs, rl, rq, rn = ref.segment_quota(p, mass, np.repeat(pads, H))
+    assert np.array_equal(ns, rn)
+    assert np.array_equal(st, rs) and np.array_equal(ln, rl) and np.array_equal(qu, rq)
+
+
+def _adversarial_masses(rng, U, T, pads, kind):
+    """Masses that drive the quota correction through its cases: peaky ones
+    (heavy short segments clipped to their length, so the rounding leaves the
+    budget over or short by many units), uniform ones (equal remainders: the
+    index tie rules decide), two-level ones (many exact ties)."""
+    m = np.zeros((U, T), np.float32)
+    for u in range(U):
+        n = T - pads[u]
+        if n <= 0:
+            continue
+        if kind == "uniform":
+            w = np.ones(n)
+        elif kind == "two_level":
+            w = np.where(rng.random(n) < 0.5, 1.0, 3.0)
+        else:
+            w = rng.random(n) ** 8
+            hot = rng.integers(0, n, rng.integers(1, 6))
+            w[hot] += rng.random(hot.size) * 50 * w.sum()
+        m[u, pads[u]:] = (w / w.sum()).astype(np.float32)
+    return m
+
+
+@pytest.mark.parametrize("kind", ["peaky", "uniform", "two_level"])
+@pytest.mark.parametrize("T,budget,delta,q_min,seg_min,seg_max", [
+    (1536, 1024, 0.1, 4, 16, 256), (1536, 200, 0.02, 8, 16, 64), (777, 700, 0.05, 4, 8, 32),
+    (2100, 2000, 0.01, 2, 4, 16)])
+def test_quota_correction_many_units(ref, kind, T, budget, delta, q_min, seg_min, seg_max):
+    """512 units per case against the oracle's one-unit-at-a-time correction,
+    bit-exact: segments, lengths and quotas."""
+    import eviction_gb300 as kvc
+    rng = np.random.default_rng(zlib.crc32(f"{kind}/{T}/{budget}".encode()))
+    B, H = 64, 8
+    pads = rng.integers(0, T // 3, B).astype(np.int32)
+    pads[:4] = 0
+    mass = _adversarial_masses(rng, B * H, T, np.repeat(pads, H), kind)
+    cfg = kvc.Config(1, B, H, 1, 64, T, budget, window=8, delta=delta, q_min=q_min,
+                     seg_min=seg_min, seg_max=seg_max)
+    h = kvc.Handle(cfg)
+    st, ln, qu, ns = gu.gpu_segment_quota(h, mass, pads, T)
+    p = ref.RefParams(group=1, head_dim=64, window=8, budget=budget, delta=delta, q_min=q_min,
                       seg_min=seg_min, seg_max=seg_max)
     rs, rl, rq, rn = ref.segment_quota(p, mass, np.repeat(pads, H))
     assert np.array_equal(ns, rn)
