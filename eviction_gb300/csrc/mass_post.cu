@@ -125,9 +125,10 @@ __global__ void __launch_bounds__(NT)
 // it there), each thread keeps its slots' values in registers across the
 // three totals, and score, mass and credit are written once.
 // Latency-bound: one CTA per unit, so the more CTAs an SM holds the better.
-// Up to 6 slots per thread it fits in 32 registers, eight CTAs per SM.
+// 32 registers: 16 CTAs of 128 threads per SM, or up to 6 slots per thread 8
+// CTAs of 256 (units past 2048 slots).
 template <int NT, int kEpt>  // T <= kEpt * NT
-__global__ void __launch_bounds__(NT, kEpt <= 6 ? 8 : (kEpt <= 8 ? 6 : 4))
+__global__ void __launch_bounds__(NT, NT == 128 ? 16 : (kEpt <= 6 ? 8 : (kEpt <= 8 ? 6 : 4)))
     mass_post_smem_kernel(PostParams p) {
   __shared__ float red[3 * (NT / 32 + 1)];
   __shared__ float a[kEpt * NT];
@@ -165,10 +166,12 @@ cudaError_t launch_mass_post(const kvc_handle* h, int T, const int32_t* pad,
   if (T <= unit::kSmemT) {
     int nt, ept;
     unit::mass_shape(T, &nt, &ept);
-    auto k = ept == 4 ? mass_post_smem_kernel<256, 4>
-             : ept == 6 ? mass_post_smem_kernel<256, 6>
-             : ept == 8 ? mass_post_smem_kernel<256, 8>
-                        : mass_post_smem_kernel<256, 16>;
+    auto k = nt == 256    ? mass_post_smem_kernel<256, 16>
+             : ept == 4  ? mass_post_smem_kernel<128, 4>
+             : ept == 6  ? mass_post_smem_kernel<128, 6>
+             : ept == 8  ? mass_post_smem_kernel<128, 8>
+             : ept == 12 ? mass_post_smem_kernel<128, 12>
+                         : mass_post_smem_kernel<128, 16>;
     k<<<dm.U, nt, 0, s>>>(p);
   } else {
     mass_post_kernel<1024><<<dm.U, 1024, 0, s>>>(p);

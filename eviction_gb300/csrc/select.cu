@@ -22,18 +22,21 @@ using unit::kRegPer;
 
 constexpr int kThreads = 256;  // units up to 4096 slots (see select_kernel)
 
-// Dynamic shared memory: start, want [S_max] | flags [T] | pick keys [budget]
-// (units past kRegPer * kThreads slots) | radix histograms [warps][256].
+// Dynamic shared memory: start, want [S_max] | flags [T] | the radix
+// histograms [warps][256] of the picks, reused by the pick keys [budget] of the
+// excess search (units past kRegPer * kThreads slots; a barrier separates the
+// two uses).
 struct SelLayout {
   int off_flag, off_key, off_hist, total;
 };
 __host__ __device__ inline SelLayout sel_layout(int S_max, int T, int budget, int warps) {
   SelLayout l;
   l.off_flag = 8 * S_max;
-  l.off_key = l.off_flag + ((T + 15) & ~15);
+  l.off_key = (l.off_flag + ((T + 15) & ~15) + 15) & ~15;
+  l.off_hist = l.off_key;
   const int keys = T > kRegPer * kThreads ? 4 * budget : 0;
-  l.off_hist = (l.off_key + keys + 15) & ~15;
-  l.total = l.off_hist + 1024 * warps;
+  const int hist = 1024 * warps;
+  l.total = l.off_key + (keys > hist ? keys : hist);
   return l;
 }
 

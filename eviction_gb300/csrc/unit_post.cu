@@ -21,9 +21,10 @@
 //   score [T] f32                mass -> selection
 //   A                            mass: filled usage [kEpt*NT] f32, then the
 //                                mass [T] f32 (written after its last read);
-//                                selection: flags [T] u8, pick keys [budget]
-//                                u32 (units past 8*NT slots), radix histograms
-//                                [NT/32][256] i32
+//                                selection: flags [T] u8, then the radix
+//                                histograms [NT/32][256] i32 of the picks, reused
+//                                by the pick keys [budget] u32 of the excess
+//                                search (units past 8*NT slots)
 //   tau [K] u64, b [K] i32       segmentation
 //   segments [S_cap] x 32 B      segmentation: mass u64 | rem i64 | start | len | q | floor;
 //                                selection: start [S_cap] | want [S_cap] over mass
@@ -48,11 +49,14 @@ struct FusedLayout {
 __host__ inline FusedLayout fused_layout(int T, int NT, int kEpt, int K, int S_cap, int budget) {
   FusedLayout l;
   l.off_a = round16(4 * T);
+  // the pick keys of the excess search and the radix histograms of the picks
+  // are never live together (a barrier separates them): one region
   l.off_key = round16(T);
+  l.off_hist = l.off_key;
   const int keys = T > unit::kRegPer * NT ? 4 * budget : 0;
-  l.off_hist = round16(l.off_key + keys);
+  const int hist = 1024 * (NT / 32);
   int a = 4 * kEpt * NT;                              // filled usage (>= the mass)
-  const int sel = l.off_hist + 1024 * (NT / 32);      // flags + keys + histograms
+  const int sel = l.off_key + (keys > hist ? keys : hist);  // flags + (keys | histograms)
   a = a > sel ? a : sel;
   l.off_tau = l.off_a + round16(a);
   l.off_seg = l.off_tau + round16(12 * K);
@@ -68,11 +72,11 @@ struct FusedParams {
 };
 
 // NT threads, kEpt = slots per thread of the mass step (unit::mass_shape).
-// Latency-bound, one CTA per unit: up to 8 slots per thread held to 32
-// registers (a few spilled), eight CTAs per SM: 0.131 -> 0.122 ms on the
-// 28-layer batch-32 event against six CTAs at 40 registers.
+// Latency-bound, one CTA per unit, held to 32 registers (some spilled) so that
+// 16 CTAs of 128 threads (or 8 of 256) share an SM: with 40 registers and 6
+// CTAs of 256 threads the 28-layer batch-32 event took 0.131 ms, 0.118 now.
 template <int NT, int kEpt>
-__global__ void __launch_bounds__(NT, kEpt <= 8 ? 8 : 4)
+__global__ void __launch_bounds__(NT, NT == 128 ? 16 : (kEpt <= 8 ? 8 : 4))
     unit_post_kernel(FusedParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ float red[3 * (NT / 32 + 1)];
@@ -213,10 +217,12 @@ cudaError_t launch_unit_post(const kvc_handle* h, int T, const int32_t* pad,
   int nt, ept;
   unit::mass_shape(T, &nt, &ept);
   p.ly = fused_layout(T, nt, ept, g.K, g.S_cap, c.budget);
-  auto kern = ept == 4   ? unit_post_kernel<256, 4>
-              : ept == 6 ? unit_post_kernel<256, 6>
-              : ept == 8 ? unit_post_kernel<256, 8>
-                         : unit_post_kernel<256, 16>;
+  auto kern = nt == 256    ? unit_post_kernel<256, 16>
+              : ept == 4  ? unit_post_kernel<128, 4>
+              : ept == 6  ? unit_post_kernel<128, 6>
+              : ept == 8  ? unit_post_kernel<128, 8>
+              : ept == 12 ? unit_post_kernel<128, 12>
+                          : unit_post_kernel<128, 16>;
   const size_t smem = static_cast<size_t>(p.ly.total);
   if (smem > 48 * 1024) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
