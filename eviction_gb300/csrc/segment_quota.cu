@@ -36,7 +36,6 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 12 : 3)
   // dynamic shared layout: seg mass (u64) | rem (i64) | start | len | quota |
   // q_floor (i32) x S_cap
   __shared__ int32_t s_b[kMaxK];
-  __shared__ uint64_t s_tau[kMaxK];
   __shared__ uint64_t s_warp[NT / 32];
   __shared__ uint64_t s_pre[NT];
   __shared__ uint64_t s_total;
@@ -49,7 +48,6 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 12 : 3)
   ss.q = ss.len + p.S_cap;
   ss.floor = ss.q + p.S_cap;
   ss.b = s_b;
-  ss.tau = s_tau;
   ss.part = s_warp;
   ss.pre = s_pre;
   ss.total = &s_total;

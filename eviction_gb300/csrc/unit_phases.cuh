@@ -296,9 +296,9 @@ struct SegParams {
 };
 
 // Shared memory of the segmentation.  mass, rem, start, len, q and floor hold
-// S_cap entries; b and tau K entries; part NT/32; pre NT.  After segment_phase returns,
+// S_cap entries; b K entries; part NT/32; pre NT.  After segment_phase returns,
 // start (valid offsets), len and q hold the unit's segments and *nseg their
-// number; mass, rem, floor, b, tau and part are free again.
+// number; mass, rem, floor, b and part are free again.
 struct SegSmem {
   uint64_t* mass;
   int64_t* rem;
@@ -307,7 +307,6 @@ struct SegSmem {
   int32_t* q;
   int32_t* floor;
   int32_t* b;
-  uint64_t* tau;
   uint64_t* part;
   uint64_t* pre;  // [NT] fixed-point mass before each thread's range
   uint64_t* total;
@@ -623,40 +622,46 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
   __syncthreads();
   const uint64_t before = sm.part[warp] + incl - local;  // prefix before `lo`
   const uint64_t S = *sm.total;
-  sm.pre[threadIdx.x] = before;
+  sm.pre[threadIdx.x] = before;  // C at the start of each thread's range
+  __syncthreads();
+  // Steps 2-6 are one short chain per unit: warp 0 runs them alone, with warp
+  // barriers only; the other warps are done.
+  if (warp != 0) return;
 
-  // ---- 2. cut points: b_k = min{t in [1,n] : C(t) >= tau_k}; each threshold
-  // is computed once (fp64 is slow on this part), then found by the thread
-  // whose range holds it
+  // ---- 2. cut points: b_k = min{t in [1,n] : C(t) >= tau_k}, lane k: the
+  // threshold once in double, then the thread range whose end first reaches it
+  // (a binary search over the range prefixes) and the slot inside that range
   const double S_d = __ull2double_rn(S);
-  for (int k = threadIdx.x; k < p.K; k += NT) {
+  for (int k = lane; k < p.K; k += 32) {
     const double frac = __dmul_rn(static_cast<double>(k + 1), p.delta);
-    sm.tau[k] = static_cast<uint64_t>(ceil(__dmul_rn(frac, S_d)));
-  }
-  __syncthreads();
-  for (int k = 0; k < p.K; ++k) {
-    const uint64_t tau = sm.tau[k];
-    if (tau == 0) {
-      if (threadIdx.x == 0) sm.b[k] = 1;
-    } else if (before < tau && tau <= before + local) {
-      uint64_t c = before;
-      for (int v = lo; v < hi; ++v) {
-        c += fixed_mass(m[v]);
-        if (c >= tau) {
-          sm.b[k] = v + 1;
-          break;
-        }
+    const uint64_t tau = static_cast<uint64_t>(ceil(__dmul_rn(frac, S_d)));
+    int bk = 1;
+    if (tau > 0) {
+      int j = 0, j_hi = NT - 1;  // the first range j with C(end of j) >= tau (C(n) = S >= tau)
+      while (j < j_hi) {
+        const int mid = (j + j_hi) >> 1;
+        const uint64_t end = mid + 1 < NT ? sm.pre[mid + 1] : S;
+        if (end >= tau) j_hi = mid; else j = mid + 1;
       }
+      uint64_t c = sm.pre[j];
+      int v = min(n, j * per);
+      const int v_end = min(n, v + per);
+      for (; v < v_end; ++v) {
+        c += fixed_mass(m[v]);
+        if (c >= tau) break;
+      }
+      bk = v + 1;
     }
+    sm.b[k] = bk;
   }
-  __syncthreads();
+  __syncwarp();
 
   // ---- 3. raw segments, merge, split (at most K+1 raw segments)
   int32_t* s_start = sm.start;
   int32_t* s_len = sm.len;
-  // (each branch condition is CTA-uniform; warp 0 runs the shuffles whole)
+  // (each branch condition is uniform; warp 0 runs the shuffles whole)
   const bool ablation = p.global_topk || p.seg_fixed > 0;
-  if (ablation && threadIdx.x == 0) {
+  if (ablation && lane == 0) {
     // ablations: one segment over everything, or fixed-length segments whose
     // shorter tail joins the segment before it
     int ns_ab = 1;
@@ -671,7 +676,7 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
       }
     }
     *sm.nseg = ns_ab;
-  } else if (!ablation && p.K < 32 && warp == 0) {
+  } else if (!ablation && p.K < 32) {
     // at most 32 raw segments: the same three rules, across warp 0.
     // Raw segments: the ends b_0 <= ... <= b_{K-1}, n; a segment where the end
     // grows (the empty ones dropped).
@@ -726,7 +731,7 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
       }
     }
     if (lane == 31) *sm.nseg = incl;
-  } else if (!ablation && p.K >= 32 && threadIdx.x == 0) {
+  } else if (!ablation && p.K >= 32 && lane == 0) {
     // raw segments into s_start/s_len (drop empty)
     int n_raw = 0, prev = 0;
     for (int k = 0; k < p.K; ++k) {
@@ -790,7 +795,7 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
     }
     *sm.nseg = n_out;
   }
-  __syncthreads();
+  __syncwarp();
   const int ns = *sm.nseg;
 
   // ---- 4. segment masses: M_s = C(end) - C(start), with C(pos) the fixed-point
@@ -803,19 +808,15 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
     for (int v = t * per; v < pos; ++v) c += fixed_mass(m[v]);
     return c;
   };
-  for (int s = threadIdx.x; s < ns; s += NT)
-    sm.mass[s] = prefix_at(s_start[s] + s_len[s]) - prefix_at(s_start[s]);
-  __syncthreads();
+  for (int s = lane; s < ns; s += 32)
+    sm.mass[s] = p.quota_by_len ? static_cast<uint64_t>(s_len[s])  // ablation: lengths for masses
+                                : prefix_at(s_start[s] + s_len[s]) - prefix_at(s_start[s]);
+  __syncwarp();
 
-  // ablation: quotas in proportion to segment length (lengths replace masses)
-  if (p.quota_by_len)
-    for (int s = threadIdx.x; s < ns; s += NT) sm.mass[s] = static_cast<uint64_t>(s_len[s]);
-  __syncthreads();
-
-  // ---- 5. quotas (warp 0)
-  if (warp == 0 && ns <= 32) {
+  // ---- 5. quotas
+  if (ns <= 32) {
     quotas_warp(p, ns, min(p.budget, n), s_len, sm.mass, sm.q, lane);
-  } else if (warp == 0) {
+  } else {
     int32_t* s_q = sm.q;
     int32_t* s_floor = sm.floor;
     const int budget = min(p.budget, n);
@@ -884,11 +885,11 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
                      reinterpret_cast<int32_t*>(sm.mass));
     }
   }
-  __syncthreads();
+  __syncwarp();
 
   // ---- 6. outputs (absolute starts), zero past n_seg
   if (write_out) {
-    for (int s = threadIdx.x; s < p.S_max; s += NT) {
+    for (int s = lane; s < p.S_max; s += 32) {
       if (s < ns) {
         o_start[s] = pad + s_start[s];
         o_len[s] = s_len[s];
@@ -899,7 +900,7 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
         o_q[s] = 0;
       }
     }
-    if (threadIdx.x == 0) p.n_seg[u] = ns;
+    if (lane == 0) p.n_seg[u] = ns;
   }
 }
 

@@ -25,7 +25,7 @@
 //                                histograms [NT/32][256] i32 of the picks, reused
 //                                by the pick keys [budget] u32 of the excess
 //                                search (units past 8*NT slots)
-//   tau [K] u64, b [K] i32       segmentation
+//   b [K] i32                    segmentation (cut points)
 //   segments [S_cap] x 32 B      segmentation: mass u64 | rem i64 | start | len | q | floor;
 //                                selection: start [S_cap] | want [S_cap] over mass
 #include "unit_phases.cuh"
@@ -42,7 +42,7 @@ constexpr int kMaxFusedT = unit::kSmemT;
 __host__ __device__ inline int round16(int x) { return (x + 15) & ~15; }
 
 struct FusedLayout {
-  int off_a, off_tau, off_seg, total;
+  int off_a, off_b, off_seg, total;
   int off_key, off_hist;  // within A, selection step
 };
 
@@ -58,8 +58,8 @@ __host__ inline FusedLayout fused_layout(int T, int NT, int kEpt, int K, int S_c
   int a = 4 * kEpt * NT;                              // filled usage (>= the mass)
   const int sel = l.off_key + (keys > hist ? keys : hist);  // flags + (keys | histograms)
   a = a > sel ? a : sel;
-  l.off_tau = l.off_a + round16(a);
-  l.off_seg = l.off_tau + round16(12 * K);
+  l.off_b = l.off_a + round16(a);
+  l.off_seg = l.off_b + round16(4 * K);
   l.total = l.off_seg + 32 * S_cap;
   return l;
 }
@@ -110,14 +110,13 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 16 : (kEpt <= 8 ? 8 : 4))
   ss.len = ss.start + S_cap;
   ss.q = ss.len + S_cap;
   ss.floor = ss.q + S_cap;
-  ss.tau = reinterpret_cast<uint64_t*>(smem + p.ly.off_tau);
-  ss.b = reinterpret_cast<int32_t*>(ss.tau + p.seg.K);
+  ss.b = reinterpret_cast<int32_t*>(smem + p.ly.off_b);
   ss.part = part;
   ss.pre = pre;
   ss.total = &total;
   ss.nseg = &nseg;
   unit::segment_phase<NT>(p.seg, u, mass_sm + pad, pad, n, ss, true);
-  __syncthreads();  // segments final; the mass is dead
+  __syncthreads();  // segments final (warp 0 wrote them); the mass is dead
 
   // Key designs 3-4: selection on the score in shared memory
   const int ns = (n > 0) ? min(nseg, p.sel.S_max) : 0;
