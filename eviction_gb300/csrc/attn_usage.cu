@@ -451,6 +451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = (tile >= 0 ? tile : 0) * BM + lrow;
         const int qpos = p.T - p.W + (r % p.W);
         const bool row_valid = tile >= 0 && (r < p.R) && (qpos >= it.pad) && (it.n_ch > 0);
+        // once per item: every row valid, and the warp's smallest query slot
+        // (a chunk's half is all visible to every row when it lies in
+        // [pad, qmin]: the per-fill test is then a few uniform compares)
+        const bool all_valid = __all_sync(0xffffffffu, row_valid);
+        const int qmin = __reduce_min_sync(0xffffffffu, qpos);
+        const int n_full = (it.c_end - it.c_start) / BN;  // chunks of BN columns
         float mz = -INFINITY, sum = 0.f;  // max in raw logit units, sum rel. to it
         for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
           if (!warp_wait(&accfull[wg], k & 1, abort, p.status)) {
@@ -459,17 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const int c0 = it.c_start + ch * BN;
-          const int n_cols = chunk_cols(it, ch);
-          const int nb = max(0, min(4, (n_cols - half * kHalf) / 32));  // this warp's blocks
-          const int lo = max(it.pad, c0), hi = min(qpos, c0 + n_cols - 1);
           const int p0 = c0 + half * kHalf;
           // every row of the warp sees all of this warp's 128 columns
-          const bool fast = __all_sync(0xffffffffu, row_valid && nb == 4 && lo <= p0 &&
-                                                        hi >= p0 + kHalf - 1);
+          const bool fast = all_valid && it.pad <= p0 && qmin >= p0 + kHalf - 1 &&
+                            (ch < n_full || chunk_cols(it, ch) - half * kHalf >= kHalf);
           uint32_t v[2][32];
           float bmx[2];
           __syncwarp();
-          if (nb == 4 && fast) {
+          if (fast) {
             // whole half, every row sees every column: two 64-column steps,
             // release after the second load
             load2(t_lane, true, v, bmx);
@@ -484,6 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // masked or partial chunk, one 32-column block at a time: a block
             // that no row of the warp sees is skipped, one that every row sees
             // in full takes the unmasked arithmetic
+            const int n_cols = chunk_cols(it, ch);
+            const int nb = max(0, min(4, (n_cols - half * kHalf) / 32));  // this warp's blocks
+            const int lo = max(it.pad, c0), hi = min(qpos, c0 + n_cols - 1);
             for (int b = 0; b < nb; ++b) {
               const int pb0 = p0 + 32 * b;
               const bool all = __all_sync(0xffffffffu, lo <= pb0 && hi >= pb0 + 31);
@@ -527,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool pos_valid = tile >= 0 && (pos >= it.pad) && (pos < p.T);
         const bool fast = __all_sync(0xffffffffu, pos_valid && (pos <= p.T - p.W));
         const int jmin = pos - (p.T - p.W);  // rows with j >= jmin see pos
+        const int n_full = (it.c_end - it.c_start) / BN;  // chunks of BN query rows
         float2 acc = make_float2(0.f, 0.f);
         for (int ch = 0; tile >= 0 && ch < it.n_ch; ++ch) {
           if (!warp_wait(&accfull[wg], k & 1, abort, p.status)) {
@@ -534,13 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const int n_cols = chunk_cols(it, ch);
-          const int nb = max(0, min(4, (n_cols - half * kHalf) / 32));
           const int r0 = ch * BN + half * kHalf;  // first query row of this warp's columns
           uint32_t v[2][32];
           float bmx[2];
           __syncwarp();
-          if (nb == 4 && fast) {
+          if (fast && (ch < n_full || chunk_cols(it, ch) - half * kHalf >= kHalf)) {
             // whole half, every query row sees the slot
             load2(t_lane, false, v, bmx);
             tmem_ld_wait();
@@ -554,6 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // one 32-row block at a time; with windows of whole blocks, a block
             // of rows that no slot of the warp is seen by is skipped and one
             // whose rows see every slot takes the unmasked arithmetic
+            const int n_cols = chunk_cols(it, ch);
+            const int nb = max(0, min(4, (n_cols - half * kHalf) / 32));
             for (int b = 0; b < nb; ++b) {
               const int rb0 = r0 + 32 * b;
               bool all = false, some = true;
