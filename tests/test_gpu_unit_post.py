@@ -106,10 +106,18 @@ def test_fused_matches_stage_chain(case):
         h.close()
 
 
-def test_event_fused_equals_stage_chain_and_compact():
-    w, T, g = _inputs("qwen_28l", dict(n_layers=2, batch=4, n_events=1))
-    h = kvc.Handle(gu.config_for(w, T))
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_event_fused_equals_stage_chain_and_compact(case):
+    """kvc_event on the fused path (mass, segments and selection in one launch,
+    then the gather) against the stage entry points and kvc_compact: compacted
+    K, V, credit, kept indices and counts bit-identical (zero rows past n_kept,
+    the all-padding sequence, head_dim 64 and 128 included)."""
+    _, name, over, pads, extra = case
+    w, T, g = _inputs(name, over, pads)
+    h = kvc.Handle(gu.config_for(w, T, **extra))
     try:
+        names = _kernels(h, lambda: gu.gpu_event(h, g, T))
+        assert names.get("mass_segment_select") == 1 and names.get("gather_compact") == 1
         ev = gu.gpu_event(h, g, T)
         sb, so = _run_stages(h, g, T)
         out = h.outputs(T)
@@ -119,6 +127,7 @@ def test_event_fused_equals_stage_chain_and_compact():
         for k in ("k_out", "v_out", "credit_out", "kept_idx", "n_kept"):
             src = out if k in ("k_out", "v_out", "credit_out") else so
             assert _same(ev[k], src[k]), k
+        assert h.device_status() == 0
     finally:
         h.close()
 
