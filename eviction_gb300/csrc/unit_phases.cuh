@@ -21,27 +21,9 @@ namespace unit {
 
 // ---------------------------------------------------------------- reductions
 
-template <int NT>
-__device__ __forceinline__ float block_sum(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  __syncthreads();  // red may still be read by a previous reduction
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float t = 0.f;
-  if (threadIdx.x < 32) {
-    t = (lane < NT / 32) ? red[lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (lane == 0) red[NT / 32] = t;
-  }
-  __syncthreads();
-  return red[NT / 32];
-}
-
-// Three block sums in one pass (the same per-warp, then fixed-order, sums as
-// block_sum).  red holds 3 * (NT/32 + 1) floats.
+// Three block sums in one pass: per-warp butterfly sums, then the warps' sums
+// in a fixed order (repeated runs give identical bits).  red holds
+// 3 * (NT/32 + 1) floats.
 template <int NT>
 __device__ __forceinline__ float3 block_sum3(float3 v, float* red) {
   constexpr int W = NT / 32;
@@ -1094,9 +1076,10 @@ struct SelSmem {
 //   * segment i picks max(0, q_i - |MK in i|) of its non-must-keep slots;
 //   * order: score descending, ties -> lower slot; removal of the excess picks
 //     in the exact reverse order (score ascending, ties -> higher slot).
-// Each warp takes whole segments: a bitwise search finds the want-th largest
-// key among the segment's candidates, then one ordered ballot pass takes the
-// ties at that key lowest slot first.  The global excess is removed the same
+// Each warp takes whole segments: a radix select (segments of up to 256 slots)
+// or a bitwise search finds the want-th largest key among the segment's
+// candidates, then one ordered ballot pass takes the ties at that key lowest
+// slot first.  The global excess is removed the same
 // way across the CTA (bitwise search for the excess-th smallest pick key, ties
 // highest slot first).  `sc` points at the unit's first valid slot.  The
 // selection compares keys only, so the result is the same for any NT.
