@@ -1118,6 +1118,14 @@ __device__ __forceinline__ void select_phase(const SelParams& p, int u, const fl
     const int en = (s + 1 < ns) ? max(st, sm.start[s + 1]) : n;
     const int want = sm.want[s];
     if (want <= 0) continue;
+    // a quota that covers the whole segment takes every candidate: no search
+    const int mk = max(0, min(en, n_s) - st) + max(0, en - max(st, n - n_r));
+    if (want >= en - st - mk) {
+      for (int v = st + lane; v < en; v += 32)
+        if (flag[v] == kOut) flag[v] = kPick;
+      __syncwarp();
+      continue;
+    }
     if (en - st <= 32 * 8)
       pick_segment_radix<kLdg>(sc, flag, st, en, want, lane, sm.hist + 256 * warp);
     else
