@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(NT)
   const float total1 = tt.x;
   const float lam = p.lambda, beta = p.beta;
   const float c_total = 1.0f + lam * (tt.y - tt.z / total1);
+  // the two normalisations as products with reciprocals taken once per unit
+  const float inv_total = 1.0f / total1;
+  const float inv_ct = c_total > 0.f ? 1.0f / c_total : 0.f;
 
   // mass (m_used) and credit
   for (int i = threadIdx.x; i < T; i += NT) {
@@ -109,9 +112,9 @@ __global__ void __launch_bounds__(NT)
     if (i >= pad) {
       float s = 0.f;
       for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
-      const float m = (fmaxf(s * inv_k, 0.f) + p.eps) / total1;
+      const float m = (fmaxf(s * inv_k, 0.f) + p.eps) * inv_total;
       c = (i < pad + n_carry) ? lam * cin[i] + (1.0f - lam) * m : m;
-      const float cn = (c_total > 0.f) ? c / c_total : m;
+      const float cn = (c_total > 0.f) ? c * inv_ct : m;
       mu = beta * m + (1.0f - beta) * cn;
     }
     mass[i] = mu;

@@ -71,6 +71,21 @@ int segment_threshold_count(double delta) {
   return K;
 }
 
+// Delta (a positive finite fp32) as m * 2^e with m odd: fl(k * Delta) in the
+// thresholds is then (k * m) * 2^e exactly (k * m < 2^35).
+void segment_delta_parts(float delta, uint64_t* m, int* e) {
+  int ex = 0;
+  const double f = std::frexp(static_cast<double>(delta), &ex);  // delta = f * 2^ex
+  uint64_t mm = static_cast<uint64_t>(std::ldexp(f, 24));  // f has 24 significant bits
+  int ee = ex - 24;
+  while (mm != 0 && (mm & 1ull) == 0) {
+    mm >>= 1;
+    ++ee;
+  }
+  *m = mm;
+  *e = ee;
+}
+
 int segment_capacity(const kvc_config& c, int T) {
   const int K = segment_threshold_count(static_cast<double>(c.delta));
   // raw segments (before merging) number at most K+1; after split/merge at
@@ -106,8 +121,8 @@ cudaError_t launch_segment_quota(const kvc_handle* h, const float* mass, int T,
   p.seg_fixed = c.seg_fixed;
   p.quota_by_len = c.quota_by_len;
   p.global_topk = c.global_topk;
-  p.delta = static_cast<double>(c.delta);
-  p.K = segment_threshold_count(p.delta);
+  segment_delta_parts(c.delta, &p.delta_m, &p.delta_e);
+  p.K = segment_threshold_count(static_cast<double>(c.delta));
   p.mass = mass;
   p.pad = pad;
   p.seg_start = seg_start;

@@ -242,15 +242,20 @@ __device__ __forceinline__ void mass_phase(const PostParams& p, int u, float* a,
   const float total1 = tt.x;
   const float lam = p.lambda, beta = p.beta;
   const float c_total = 1.0f + lam * (tt.y - tt.z / total1);
+  // the two normalisations as products with reciprocals taken once per unit
+  // (an IEEE division per slot costs about ten instructions; the product is
+  // within an ulp of the quotient)
+  const float inv_total = 1.0f / total1;
+  const float inv_ct = c_total > 0.f ? 1.0f / c_total : 0.f;
 #pragma unroll
   for (int k = 0; k < kEpt; ++k) {
     const int i = tid + k * NT;
     if (i >= T) continue;
     float mu = 0.f, c = 0.f;
     if (i >= pad) {
-      const float m = up[k] / total1;
+      const float m = up[k] * inv_total;
       c = (i < pad + n_carry) ? lam * cprior[k] + (1.0f - lam) * m : m;
-      const float cn = (c_total > 0.f) ? c / c_total : m;
+      const float cn = (c_total > 0.f) ? c * inv_ct : m;
       mu = beta * m + (1.0f - beta) * cn;
     }
     mass[i] = mu;
@@ -267,7 +272,8 @@ struct SegParams {
   int T, B, H, S_max, S_cap;
   int budget, q_min, seg_min, seg_max;
   int seg_fixed, quota_by_len, global_topk;  // ablation switches (0 = the method)
-  double delta;
+  uint64_t delta_m;  // Delta = delta_m * 2^delta_e, delta_m odd (the fp32 Delta's significand)
+  int delta_e;
   int K;  // number of thresholds
   const float* mass;
   const int32_t* pad;
@@ -299,6 +305,40 @@ __device__ __forceinline__ uint64_t fixed_mass(float m) {
   // m * 2^40 is exact in fp32 (an exponent shift); truncation toward zero.
   const float scaled = m * 1099511627776.0f;
   return scaled > 0.f ? __float2ull_rz(scaled) : 0ull;
+}
+
+// x rounded to 53 significant bits (IEEE round to nearest, ties to even) as
+// q * 2^r, q <= 2^53; x < 2^88 given as hi:lo, so r <= 35.
+__device__ __forceinline__ uint64_t round53(uint64_t lo, uint64_t hi, int* r_out) {
+  const int nb = hi ? 128 - __clzll(hi) : 64 - __clzll(lo);
+  if (nb <= 53) {
+    *r_out = 0;
+    return lo;
+  }
+  const int r = nb - 53;
+  uint64_t q = (lo >> r) | (hi << (64 - r));
+  const bool g = (lo >> (r - 1)) & 1ull;                               // the first bit dropped
+  const bool sticky = r > 1 && (lo & ((1ull << (r - 1)) - 1ull)) != 0ull;  // any bit below it
+  if (g && (sticky || (q & 1ull))) ++q;
+  *r_out = r;
+  return q;
+}
+
+// ceil(fl(fl(A * 2^eA) * fl(S))) in IEEE double for A < 2^35 and
+// A * 2^eA < 1: fl(A * 2^eA) is exact, fl(S) is S rounded to 53 significant
+// bits, and the product of the two significands (below 2^88) is rounded to 53
+// bits once; the ceiling of the result.  Integers only, and bit for bit the
+// double computation (double arithmetic is a slow path on this GPU).
+__device__ __forceinline__ uint64_t ceil_scaled_product(uint64_t A, int eA, uint64_t S) {
+  if (A == 0ull || S == 0ull) return 0ull;
+  int ts, r;
+  const uint64_t qs = round53(S, 0ull, &ts);
+  const uint64_t q = round53(A * qs, __umul64hi(A, qs), &r);
+  const int t = eA + ts + r;  // the rounded product is q * 2^t
+  if (t >= 0) return q << t;  // (below S: A * 2^eA < 1)
+  const int s = -t;
+  if (s >= 64) return 1ull;
+  return (q >> s) + ((q & ((1ull << s) - 1ull)) ? 1ull : 0ull);
 }
 
 __device__ __forceinline__ uint64_t warp_incl_scan(uint64_t v) {
@@ -412,11 +452,19 @@ __device__ __forceinline__ void take_best_bids(const int64_t* rem, const int32_t
   __syncwarp();
 }
 
+// x as an fp32 estimate (relative error below 2^-22) from two 32-bit
+// conversions: 64-bit conversions are far slower on this GPU.
+__device__ __forceinline__ float u64_to_f32_est(uint64_t x) {
+  return __fmaf_rn(__uint2float_rn(static_cast<uint32_t>(x >> 32)), 4294967296.0f,
+                   __uint2float_rn(static_cast<uint32_t>(x)));
+}
+
 // floor(num / den) for 0 <= num, 0 < den, with num / den < 2^24: an fp32
-// estimate corrected by exact integer multiplication (products below 2^63).
+// estimate (off by a few units at most) corrected by exact integer
+// multiplication (products below 2^63).
 __device__ __forceinline__ uint64_t udiv_small(uint64_t num, uint64_t den) {
-  uint64_t q = static_cast<uint64_t>(
-      fmaxf(0.f, __fdividef(__ull2float_rz(num), __ull2float_rz(den))));
+  uint64_t q = __float2uint_rz(
+      fminf(16777216.f, fmaxf(0.f, __fdividef(u64_to_f32_est(num), u64_to_f32_est(den)))));
   while (q > 0 && q * den > num) --q;
   while ((q + 1) * den <= num) ++q;
   return q;
@@ -424,8 +472,11 @@ __device__ __forceinline__ uint64_t udiv_small(uint64_t num, uint64_t den) {
 
 // floor(num / den) for 0 < den, |num / den| < 2^24, likewise.
 __device__ __forceinline__ int64_t sdiv_floor_small(int64_t num, int64_t den) {
-  int64_t q = static_cast<int64_t>(floorf(__fdividef(static_cast<float>(num),
-                                                       static_cast<float>(den))));
+  const uint64_t a = num < 0 ? static_cast<uint64_t>(-num) : static_cast<uint64_t>(num);
+  const float e = fminf(16777216.f, __fdividef(u64_to_f32_est(a),
+                                               u64_to_f32_est(static_cast<uint64_t>(den))));
+  const int64_t m = static_cast<int64_t>(__float2uint_rz(e));
+  int64_t q = num < 0 ? -m : m;
   while (q * den > num) --q;
   while ((q + 1) * den <= num) ++q;
   return q;
@@ -549,9 +600,9 @@ __device__ __forceinline__ void quotas_warp(const SP& p, int ns, int budget,
 // Exactness: the fp32 mass becomes 40-bit fixed point (mu = trunc(m * 2^40),
 // exact), prefix sums are uint64, the thresholds are
 // tau_k = ceil(fl(fl(k*Delta) * S)) in IEEE double with round-to-nearest and no
-// fused operations, the split/merge and quota rules are integer only.  The
-// same definitions with the same tie rules give the same bits on any machine
-// and for any NT.
+// fused operations (evaluated exactly so in integers by ceil_scaled_product),
+// the split/merge and quota rules are integer only.  The same definitions with
+// the same tie rules give the same bits on any machine and for any NT.
 //   * empty raw segments are dropped; merge left to right until >= seg_min,
 //     a short tail joins its predecessor; then split L > seg_max into
 //     c = ceil(L/seg_max) parts, the first L mod c one longer;
@@ -611,12 +662,12 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
   if (warp != 0) return;
 
   // ---- 2. cut points: b_k = min{t in [1,n] : C(t) >= tau_k}, lane k: the
-  // threshold once in double, then the thread range whose end first reaches it
-  // (a binary search over the range prefixes) and the slot inside that range
-  const double S_d = __ull2double_rn(S);
+  // threshold (the double computation, in integers), then the thread range
+  // whose end first reaches it (a binary search over the range prefixes) and
+  // the slot inside that range; n if no prefix reaches it
   for (int k = lane; k < p.K; k += 32) {
-    const double frac = __dmul_rn(static_cast<double>(k + 1), p.delta);
-    const uint64_t tau = static_cast<uint64_t>(ceil(__dmul_rn(frac, S_d)));
+    const uint64_t tau =
+        ceil_scaled_product(static_cast<uint64_t>(k + 1) * p.delta_m, p.delta_e, S);
     int bk = 1;
     if (tau > 0) {
       int j = 0, j_hi = NT - 1;  // the first range j with C(end of j) >= tau (C(n) = S >= tau)
@@ -632,7 +683,7 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
         c += fixed_mass(m[v]);
         if (c >= tau) break;
       }
-      bk = v + 1;
+      bk = min(v + 1, n);
     }
     sm.b[k] = bk;
   }

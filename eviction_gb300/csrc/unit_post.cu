@@ -33,6 +33,7 @@
 namespace kvc {
 int attention_row_stride(int R);
 int segment_threshold_count(double delta);
+void segment_delta_parts(float delta, uint64_t* m, int* e);
 int segment_capacity(const kvc_config& c, int T);
 
 namespace {
@@ -189,8 +190,8 @@ cudaError_t launch_unit_post(const kvc_handle* h, int T, const int32_t* pad,
   g.seg_fixed = c.seg_fixed;
   g.quota_by_len = c.quota_by_len;
   g.global_topk = c.global_topk;
-  g.delta = static_cast<double>(c.delta);
-  g.K = segment_threshold_count(g.delta);
+  segment_delta_parts(c.delta, &g.delta_m, &g.delta_e);
+  g.K = segment_threshold_count(static_cast<double>(c.delta));
   g.mass = mass;
   g.pad = pad;
   g.seg_start = seg_start;

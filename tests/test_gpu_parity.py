@@ -24,6 +24,7 @@ import workload as wl
 pytestmark = pytest.mark.gpu
 
 from tests import gpu_util as gu  # noqa: E402
+from tests import threshold_cases  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -177,6 +178,40 @@ def test_quota_correction_many_units(ref, kind, T, budget, delta, q_min, seg_min
     rs, rl, rq, rn = ref.segment_quota(p, mass, np.repeat(pads, H))
     assert np.array_equal(ns, rn)
     assert np.array_equal(st, rs) and np.array_equal(ln, rl) and np.array_equal(qu, rq)
+
+
+@pytest.mark.parametrize("delta", [0.1, 0.07, 0.013])
+def test_segment_thresholds_on_rounding_cases(ref, delta):
+    """Masses whose cut points sit on tau_k - 1 and tau_k exactly, with tau_k
+    where the double rounding of k*Delta*S decides it (below half of the last
+    bit, ties to even and odd, exact, just under a bit): the segments, lengths
+    and quotas bit-identical to the oracle's, and every crafted cut where the
+    double threshold puts it (a threshold one off either way moves it)."""
+    import eviction_gb300 as kvc
+    rng = np.random.default_rng(zlib.crc32(f"thresholds/{delta}".encode()))
+    T, B, H, budget = 4096, 10, 4, 700
+    K = threshold_cases.threshold_count(delta)
+    ks = [k for k in range(1, K + 1) if threshold_cases.usable(k, delta)]
+    pads = rng.integers(0, T - 1536 + 1, B).astype(np.int32)
+    pads[0] = 0
+    mass = np.zeros((B * H, T), np.float32)
+    crafted = []
+    for u in range(B * H):
+        pad = int(pads[u // H])
+        c = threshold_cases.craft(rng, T - pad, int(rng.choice(ks)), delta,
+                                  threshold_cases.KINDS[u % len(threshold_cases.KINDS)])
+        mass[u, pad:] = c.mass_f32()
+        crafted.append((pad, c))
+    cfg = kvc.Config(1, B, H, 1, 64, T, budget, window=8, delta=delta, seg_min=1, seg_max=4096)
+    h = kvc.Handle(cfg)
+    st, ln, qu, ns = gu.gpu_segment_quota(h, mass, pads, T)
+    p = ref.RefParams(group=1, head_dim=64, window=8, budget=budget, delta=delta, seg_min=1,
+                      seg_max=4096)
+    rs, rl, rq, rn = ref.segment_quota(p, mass, np.repeat(pads, H))
+    assert np.array_equal(ns, rn)
+    assert np.array_equal(st, rs) and np.array_equal(ln, rl) and np.array_equal(qu, rq)
+    for u, (pad, c) in enumerate(crafted):  # no merging or splitting here: raw cuts
+        assert pad + c.t0 in set(st[u, :ns[u]].tolist()), (u, c.kind, c.k)
 
 
 @pytest.mark.parametrize("name", list(CASES))

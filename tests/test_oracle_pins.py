@@ -2,18 +2,22 @@
 
 Nothing here compares the oracle with itself: every expected value comes from a
 closed form, a library routine (torch softmax / pooling / index_select, numpy
-sort), exact rational arithmetic, brute-force enumeration or the worked example
+sort), exact rational arithmetic, Python's own IEEE doubles, brute-force
+enumeration or the worked example
 of "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning" (section
 "A complete example").
 """
 import itertools
 import math
 import os
+import zlib
 from fractions import Fraction
 
 import numpy as np
 import pytest
 import torch
+
+from tests import threshold_cases
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -247,6 +251,31 @@ def test_boundaries_match_exact_rule(ref, seed, n):
         near_raw = any(abs(c - k * d) < abs(total - 1) + Fraction(1, 10 ** 7) for c in C)
         if rk is not None and not near_raw:
             assert bk == rk, (k, bk, rk)
+
+
+@pytest.mark.parametrize("delta", [0.1, 0.07, 0.013])
+@pytest.mark.parametrize("kind", threshold_cases.KINDS)
+def test_boundaries_round_thresholds_as_double(ref, delta, kind):
+    """The reading that fixes the cut points bit for bit: tau_k =
+    ceil(fl(fl(k*Delta) * S)) in IEEE double, ties to even.  On masses whose
+    prefix sums sit on tau_k - 1 and tau_k where that rounding decides (the
+    double threshold one below the exact ceiling for "below" and "tie_even"),
+    the oracle cuts exactly where Python's doubles put the threshold, and a
+    threshold one off either way would cut elsewhere."""
+    rng = np.random.default_rng(zlib.crc32(f"{delta}/{kind}".encode()))
+    K = threshold_cases.threshold_count(delta)
+    ks = [k for k in range(1, K + 1) if threshold_cases.usable(k, delta)]
+    for k in sorted({ks[0], ks[-1], ks[len(ks) // 2], int(rng.choice(ks))}):
+        c = threshold_cases.craft(rng, int(rng.integers(1536, 4097)), k, delta, kind)
+        m = c.mass_f32()
+        b, total = ref.boundaries(m, 0, delta)
+        assert total == c.S and len(b) == K
+        assert b[k - 1] == c.t0
+        C = np.cumsum(c.mu)
+        cut = lambda tau: int(np.searchsorted(C, tau)) + 1  # min{t : C(t) >= tau}
+        assert cut(c.tau - 1) == c.t0 - 1 and cut(c.tau + 1) == c.t0 + 1
+        exact = threshold_cases.tau_exact(k, delta, c.S)
+        assert cut(exact) == (c.t0 + 1 if kind in ("below", "tie_even") else c.t0)
 
 
 def test_segmentation_golden(ref):
