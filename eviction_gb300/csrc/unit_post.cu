@@ -3,11 +3,13 @@
 //
 // "Adaptive Mass-Segmented KV Compression for Long-Form Reasoning", Method,
 // Key designs 1-4, and its overhead statement: after the attention usage, mass
-// processing and the prefix sum are O(H_kv * T) work per layer.  That work is
-// latency-bound (block reductions, a scan, a serial segment build, searches),
-// so the three steps share one launch, and the unit's mass, score and segments
-// stay in shared memory between them instead of making a round trip through
-// global memory between three launches.
+// processing and the prefix sum are O(H_kv * T) work per layer.  That work is a
+// chain of short dependent steps per unit (block reductions, a scan, a serial
+// segment build, searches), so the three steps share one launch, and the
+// unit's mass, score and segments stay in shared memory between them instead
+// of making a round trip through global memory between three launches.  With
+// 15 CTAs per SM the schedulers are busy most of the time: the kernel's time
+// follows its instruction count.
 //
 // The steps are the functions of unit_phases.cuh that the stand-alone kernels
 // run, with the CTA shape of the stand-alone mass kernel (unit::mass_shape; the
