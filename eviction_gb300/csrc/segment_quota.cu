@@ -23,6 +23,10 @@ using unit::SegParams;
 using unit::kMaxK;
 
 constexpr int kThreads = 128;  // per-unit latency chains: more CTAs in flight beat wider ones
+// Units longer than 4096 slots: 8 sub-range prefixes per thread range (64 slots
+// of a 32768-slot unit each), so warp 0's scans of the mass in global memory
+// (cut points, segment masses) cover 8 slots instead of 64.
+constexpr int kLongSub = 8;
 
 // NT = 128: 12 CTAs per SM (40 registers) rather than 10 at the natural 48:
 // the kernel is latency-bound per unit, and more units in flight shorten the
@@ -38,6 +42,7 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 12 : 3)
   __shared__ int32_t s_b[kMaxK];
   __shared__ uint64_t s_warp[NT / 32];
   __shared__ uint64_t s_pre[NT];
+  __shared__ uint64_t s_sub[NT == 512 ? NT * kLongSub : 1];
   __shared__ uint64_t s_total;
   __shared__ int s_nseg;
   unit::SegSmem ss;
@@ -50,14 +55,15 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 12 : 3)
   ss.b = s_b;
   ss.part = s_warp;
   ss.pre = s_pre;
+  ss.sub = s_sub;
   ss.total = &s_total;
   ss.nseg = &s_nseg;
   const int u = blockIdx.x;
   const int T = p.T;
   const int b = (u / p.H) % p.B;
   const int pad = min(max(p.pad[b], 0), T);
-  unit::segment_phase<NT>(p, u, p.mass + static_cast<size_t>(u) * T + pad, pad, T - pad, ss,
-                          true);
+  unit::segment_phase<NT, NT == 512 ? kLongSub : 1>(p, u, p.mass + static_cast<size_t>(u) * T + pad,
+                                                    pad, T - pad, ss, true);
 }
 
 }  // namespace

@@ -285,7 +285,8 @@ struct SegParams {
 };
 
 // Shared memory of the segmentation.  mass, rem, start, len, q and floor hold
-// S_cap entries; b K entries; part NT/32; pre NT.  After segment_phase returns,
+// S_cap entries; b K entries; part NT/32; pre NT; sub NT*kSub when
+// segment_phase runs with kSub > 1 (else unused).  After segment_phase returns,
 // start (valid offsets), len and q hold the unit's segments and *nseg their
 // number; mass, rem, floor, b and part are free again.
 struct SegSmem {
@@ -298,6 +299,7 @@ struct SegSmem {
   int32_t* b;
   uint64_t* part;
   uint64_t* pre;  // [NT] fixed-point mass before each thread's range
+  uint64_t* sub;  // [NT][kSub] the same before each of its kSub sub-ranges
   uint64_t* total;
   int* nseg;
 };
@@ -352,6 +354,36 @@ __device__ __forceinline__ uint64_t warp_incl_scan(uint64_t v) {
   return v;
 }
 
+// x as an fp32 estimate (relative error below 2^-22) from two 32-bit
+// conversions: 64-bit conversions are far slower on this GPU.
+__device__ __forceinline__ float u64_to_f32_est(uint64_t x) {
+  return __fmaf_rn(__uint2float_rn(static_cast<uint32_t>(x >> 32)), 4294967296.0f,
+                   __uint2float_rn(static_cast<uint32_t>(x)));
+}
+
+// floor(num / den) for 0 <= num, 0 < den, with num / den < 2^24: an fp32
+// estimate (off by a few units at most) corrected by exact integer
+// multiplication (products below 2^63).
+__device__ __forceinline__ uint64_t udiv_small(uint64_t num, uint64_t den) {
+  uint64_t q = __float2uint_rz(
+      fminf(16777216.f, fmaxf(0.f, __fdividef(u64_to_f32_est(num), u64_to_f32_est(den)))));
+  while (q > 0 && q * den > num) --q;
+  while ((q + 1) * den <= num) ++q;
+  return q;
+}
+
+// floor(num / den) for 0 < den, |num / den| < 2^24, likewise.
+__device__ __forceinline__ int64_t sdiv_floor_small(int64_t num, int64_t den) {
+  const uint64_t a = num < 0 ? static_cast<uint64_t>(-num) : static_cast<uint64_t>(num);
+  const float e = fminf(16777216.f, __fdividef(u64_to_f32_est(a),
+                                               u64_to_f32_est(static_cast<uint64_t>(den))));
+  const int64_t m = static_cast<int64_t>(__float2uint_rz(e));
+  int64_t q = num < 0 ? -m : m;
+  while (q * den > num) --q;
+  while ((q + 1) * den <= num) ++q;
+  return q;
+}
+
 // The correction steps of the quota rule, in bulk.  Each step gives (or takes)
 // one unit to the segment with the best current remainder, and a segment's
 // remainder moves by the mass total M per unit, so the steps taken are exactly
@@ -364,10 +396,14 @@ __device__ __forceinline__ uint64_t warp_incl_scan(uint64_t v) {
 // levels j_s - k, k < cap_s, with j_s = floor((b0_s + h) / M) its first bid's.
 // The D best bids are all bids above the level L at which the count from the
 // top reaches D (a binary search on small integers), plus the D' best bids of
-// level L in (value, index) order.  One 64-bit division per segment; counts
-// are 32-bit (they are at most the unit's slot count).  `scratch` holds 2*ns
-// int32: the segments' first levels, then the units taken.
-__device__ __forceinline__ void take_best_bids(const int64_t* rem, const int32_t* ref, int32_t* q,
+// level L in (value, index) order.  A segment's bid at level L is
+// (L*M - h) + w_s with w_s = (b0_s + h) - j_s*M in [0, M), the remainder of
+// its level division, so level L's bids order as their w: a bitwise search
+// finds the D'-th largest w among the segments with a bid there, and the ties
+// at it go in index order.  One small division per segment; counts are 32-bit
+// (they are at most the unit's slot count).  `scratch` holds 2*ns int32: the
+// segments' first levels, then the units taken; `rem` is overwritten with w.
+__device__ __forceinline__ void take_best_bids(int64_t* rem, const int32_t* ref, int32_t* q,
                                                int ns, int64_t M, int D, bool negate,
                                                bool low_first, int lane, int32_t* scratch) {
   int32_t* lev = scratch;
@@ -399,15 +435,16 @@ __device__ __forceinline__ void take_best_bids(const int64_t* rem, const int32_t
     for (int s = lane; s < ns; s += 32) {
       const int cap = cap_of(s);
       int j = 0;
+      int64_t w = 0;
       if (cap > 0) {
         const int64_t num = b0_of(s) + h;
-        int64_t jj = num / M;  // toward zero; floor for negative num:
-        if (num % M != 0 && num < 0) --jj;
-        j = static_cast<int>(jj);
+        j = static_cast<int>(sdiv_floor_small(num, M));
+        w = num - static_cast<int64_t>(j) * M;
         lo = min(lo, j - cap + 1);
         hi = max(hi, j);
       }
       lev[s] = j;
+      rem[s] = w;  // b0 is not needed again
     }
     lo = __reduce_min_sync(0xffffffffu, lo);
     hi = __reduce_max_sync(0xffffffffu, hi);
@@ -428,24 +465,46 @@ __device__ __forceinline__ void take_best_bids(const int64_t* rem, const int32_t
       if (count_ge(mid) >= D) L = mid; else L_hi = mid - 1;
     }
     const int d_at_L = D - count_ge(L + 1);  // bids taken at level L
+    auto at_L = [&](int s) {  // segment s has a bid at level L
+      const int cap = cap_of(s);
+      return cap > 0 && lev[s] - cap < L && L <= lev[s];
+    };
     for (int s = lane; s < ns; s += 32) {
       const int cap = cap_of(s);
-      int t = 0;
-      if (cap > 0) {
-        t = max(0, min(cap, lev[s] - L));  // bids above level L
-        if (d_at_L > 0 && lev[s] - cap < L && L <= lev[s]) {
-          const int64_t v = b0_of(s) - static_cast<int64_t>(lev[s] - L) * M;
-          int rank = 0;
-          for (int j = 0; j < ns; ++j) {
-            const int capj = cap_of(j);
-            if (j == s || capj <= 0 || !(lev[j] - capj < L && L <= lev[j])) continue;
-            const int64_t vj = b0_of(j) - static_cast<int64_t>(lev[j] - L) * M;
-            rank += (vj > v || (vj == v && (low_first ? j < s : j > s))) ? 1 : 0;
-          }
-          if (rank < d_at_L) t += 1;
-        }
+      take[s] = cap > 0 ? max(0, min(cap, lev[s] - L)) : 0;  // bids above level L
+    }
+    if (d_at_L > 0) {  // warp-uniform
+      // x = the d_at_L-th largest w at level L: the largest x with
+      // #(w >= x) >= d_at_L
+      uint64_t x = 0;
+      for (int bit = 63 - __clzll(static_cast<uint64_t>(M)); bit >= 0; --bit) {  // w < M
+        const uint64_t t = x | (1ull << bit);
+        int c = 0;
+        for (int s = lane; s < ns; s += 32)
+          c += (at_L(s) && static_cast<uint64_t>(rem[s]) >= t) ? 1 : 0;
+        if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c))) >= d_at_L)
+          x = t;
       }
-      take[s] = t;
+      int gt = 0;
+      for (int s = lane; s < ns; s += 32)
+        gt += (at_L(s) && static_cast<uint64_t>(rem[s]) > x) ? 1 : 0;
+      int ties_left = d_at_L - static_cast<int>(__reduce_add_sync(0xffffffffu,
+                                                                   static_cast<unsigned>(gt)));
+      // every bid above x, then the ties at x in index order (lower first when
+      // short, higher first when over), 32 segments at a time
+      const int n_chunks = (ns + 31) / 32;
+      const uint32_t ahead = low_first ? ((1u << lane) - 1u)
+                                       : (lane == 31 ? 0u : (0xffffffffu << (lane + 1)));
+      for (int cc = 0; cc < n_chunks; ++cc) {
+        const int s = (low_first ? cc : n_chunks - 1 - cc) * 32 + lane;
+        const bool in = s < ns && at_L(s);
+        const uint64_t w = in ? static_cast<uint64_t>(rem[s]) : 0ull;
+        const bool tie = in && w == x;
+        const uint32_t ball = __ballot_sync(0xffffffffu, tie);
+        if ((in && w > x) || (tie && static_cast<int>(__popc(ball & ahead)) < ties_left))
+          take[s] += 1;
+        ties_left -= __popc(ball);
+      }
     }
   }
   __syncwarp();
@@ -453,34 +512,10 @@ __device__ __forceinline__ void take_best_bids(const int64_t* rem, const int32_t
   __syncwarp();
 }
 
-// x as an fp32 estimate (relative error below 2^-22) from two 32-bit
-// conversions: 64-bit conversions are far slower on this GPU.
-__device__ __forceinline__ float u64_to_f32_est(uint64_t x) {
-  return __fmaf_rn(__uint2float_rn(static_cast<uint32_t>(x >> 32)), 4294967296.0f,
-                   __uint2float_rn(static_cast<uint32_t>(x)));
-}
-
-// floor(num / den) for 0 <= num, 0 < den, with num / den < 2^24: an fp32
-// estimate (off by a few units at most) corrected by exact integer
-// multiplication (products below 2^63).
-__device__ __forceinline__ uint64_t udiv_small(uint64_t num, uint64_t den) {
-  uint64_t q = __float2uint_rz(
-      fminf(16777216.f, fmaxf(0.f, __fdividef(u64_to_f32_est(num), u64_to_f32_est(den)))));
-  while (q > 0 && q * den > num) --q;
-  while ((q + 1) * den <= num) ++q;
-  return q;
-}
-
-// floor(num / den) for 0 < den, |num / den| < 2^24, likewise.
-__device__ __forceinline__ int64_t sdiv_floor_small(int64_t num, int64_t den) {
-  const uint64_t a = num < 0 ? static_cast<uint64_t>(-num) : static_cast<uint64_t>(num);
-  const float e = fminf(16777216.f, __fdividef(u64_to_f32_est(a),
-                                               u64_to_f32_est(static_cast<uint64_t>(den))));
-  const int64_t m = static_cast<int64_t>(__float2uint_rz(e));
-  int64_t q = num < 0 ? -m : m;
-  while (q * den > num) --q;
-  while ((q + 1) * den <= num) ++q;
-  return q;
+__device__ __forceinline__ int64_t shfl64_down(int64_t v) {  // lane + 1's value (lane 31: its own)
+  const int lo = __shfl_down_sync(0xffffffffu, static_cast<int>(v & 0xffffffff), 1);
+  const int hi = __shfl_down_sync(0xffffffffu, static_cast<int>(v >> 32), 1);
+  return (static_cast<int64_t>(hi) << 32) | static_cast<uint32_t>(lo);
 }
 
 __device__ __forceinline__ int64_t shfl64(int64_t v, int src) {
@@ -613,8 +648,11 @@ __device__ __forceinline__ void quotas_warp(const SP& p, int ns, int budget,
 //     over: smallest remainder among q > q^min, ties higher index).
 // `m` points at the unit's first valid slot (n = T - pad of them), in global or
 // shared memory.  With `write_out` the segments (absolute starts), lengths,
-// quotas and count go to the global arrays, zero past the count.
-template <int NT>
+// quotas and count go to the global arrays, zero past the count.  kSub > 1
+// keeps the prefix at kSub sub-ranges of every thread's range too (sm.sub), so
+// that the warp's later scans of `m` (long units: in global memory) cover one
+// sub-range at most.
+template <int NT, int kSub = 1>
 __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const float* m, int pad,
                                               int n, const SegSmem& sm, bool write_out) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -637,10 +675,20 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
   }
 
   // ---- 1. prefix sums of the fixed-point mass over contiguous thread ranges
+  // (and, with kSub > 1, over kSub sub-ranges of g slots in each)
   const int per = (n + NT - 1) / NT;
+  const int g = (per + kSub - 1) / kSub;
   const int lo = min(n, static_cast<int>(threadIdx.x) * per), hi = min(n, lo + per);
   uint64_t local = 0;
-  for (int v = lo; v < hi; ++v) local += fixed_mass(m[v]);
+  if constexpr (kSub > 1) {
+    for (int j = 0; j < kSub; ++j) {
+      sm.sub[threadIdx.x * kSub + j] = local;  // relative to the range's start for now
+      const int e = min(hi, lo + (j + 1) * g);
+      for (int v = min(hi, lo + j * g); v < e; ++v) local += fixed_mass(m[v]);
+    }
+  } else {
+    for (int v = lo; v < hi; ++v) local += fixed_mass(m[v]);
+  }
   const uint64_t incl = warp_incl_scan(local);
   if (lane == 31) sm.part[warp] = incl;
   __syncthreads();
@@ -657,29 +705,37 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
   const uint64_t before = sm.part[warp] + incl - local;  // prefix before `lo`
   const uint64_t S = *sm.total;
   sm.pre[threadIdx.x] = before;  // C at the start of each thread's range
+  if constexpr (kSub > 1) {
+#pragma unroll
+    for (int j = 0; j < kSub; ++j) sm.sub[threadIdx.x * kSub + j] += before;
+  }
   __syncthreads();
   // Steps 2-6 are one short chain per unit: warp 0 runs them alone, with warp
   // barriers only; the other warps are done.
   if (warp != 0) return;
 
   // ---- 2. cut points: b_k = min{t in [1,n] : C(t) >= tau_k}, lane k: the
-  // threshold (the double computation, in integers), then the thread range
-  // whose end first reaches it (a binary search over the range prefixes) and
-  // the slot inside that range; n if no prefix reaches it
+  // threshold (the double computation, in integers), then the range (thread
+  // range, or sub-range with kSub > 1) whose end first reaches it (a binary
+  // search over the range prefixes) and the slot inside that range; n if no
+  // prefix reaches it
+  constexpr int kRanges = NT * kSub;
+  const uint64_t* range_pre = kSub > 1 ? sm.sub : sm.pre;
   for (int k = lane; k < p.K; k += 32) {
     const uint64_t tau =
         ceil_scaled_product(static_cast<uint64_t>(k + 1) * p.delta_m, p.delta_e, S);
     int bk = 1;
     if (tau > 0) {
-      int j = 0, j_hi = NT - 1;  // the first range j with C(end of j) >= tau (C(n) = S >= tau)
+      int j = 0, j_hi = kRanges - 1;  // the first range j with C(end of j) >= tau (C(n) = S >= tau)
       while (j < j_hi) {
         const int mid = (j + j_hi) >> 1;
-        const uint64_t end = mid + 1 < NT ? sm.pre[mid + 1] : S;
+        const uint64_t end = mid + 1 < kRanges ? range_pre[mid + 1] : S;
         if (end >= tau) j_hi = mid; else j = mid + 1;
       }
-      uint64_t c = sm.pre[j];
-      int v = min(n, j * per);
-      const int v_end = min(n, v + per);
+      uint64_t c = range_pre[j];
+      const int t_lo = min(n, (j / kSub) * per), t_hi = min(n, t_lo + per);
+      int v = min(t_hi, t_lo + (j % kSub) * g);
+      const int v_end = kSub > 1 ? min(t_hi, t_lo + (j % kSub + 1) * g) : t_hi;
       for (; v < v_end; ++v) {
         c += fixed_mass(m[v]);
         if (c >= tau) break;
@@ -833,18 +889,37 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
   const int ns = *sm.nseg;
 
   // ---- 4. segment masses: M_s = C(end) - C(start), with C(pos) the fixed-point
-  // mass of the first pos valid slots from the thread-range prefixes of step 1
-  // (the same integer sums, in another order: exact)
+  // mass of the first pos valid slots from the range prefixes of step 1 (the
+  // same integer sums, in another order: exact).  The segments tile [0, n), so
+  // a segment ends where the next starts: C is taken once per start.
   auto prefix_at = [&](int pos) -> uint64_t {
     if (pos >= n) return S;
     const int t = pos / per;
-    uint64_t c = sm.pre[t];
-    for (int v = t * per; v < pos; ++v) c += fixed_mass(m[v]);
+    int v = t * per;
+    uint64_t c;
+    if constexpr (kSub > 1) {
+      const int j = (pos - v) / g;
+      c = sm.sub[t * kSub + j];
+      v += j * g;
+    } else {
+      c = sm.pre[t];
+    }
+    for (; v < pos; ++v) c += fixed_mass(m[v]);
     return c;
   };
-  for (int s = lane; s < ns; s += 32)
-    sm.mass[s] = p.quota_by_len ? static_cast<uint64_t>(s_len[s])  // ablation: lengths for masses
-                                : prefix_at(s_start[s] + s_len[s]) - prefix_at(s_start[s]);
+  if (p.quota_by_len) {  // ablation: lengths for masses
+    for (int s = lane; s < ns; s += 32) sm.mass[s] = static_cast<uint64_t>(s_len[s]);
+  } else if (ns <= 32) {  // one segment per lane
+    const uint64_t c0 = lane < ns ? prefix_at(s_start[lane]) : 0ull;
+    const uint64_t c1 = static_cast<uint64_t>(shfl64_down(static_cast<int64_t>(c0)));
+    if (lane < ns) sm.mass[lane] = (lane + 1 < ns ? c1 : S) - c0;
+  } else {  // C at every start into rem (free until step 5), then the differences
+    for (int s = lane; s < ns; s += 32) sm.rem[s] = static_cast<int64_t>(prefix_at(s_start[s]));
+    __syncwarp();
+    for (int s = lane; s < ns; s += 32)
+      sm.mass[s] = (s + 1 < ns ? static_cast<uint64_t>(sm.rem[s + 1]) : S) -
+                   static_cast<uint64_t>(sm.rem[s]);
+  }
   __syncwarp();
 
   // ---- 5. quotas
@@ -889,7 +964,7 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
       int64_t share = 0;
       if (Mt > 0) {
         const uint64_t num = 2ull * static_cast<uint64_t>(t_rem) * sm.mass[s] + Mt;
-        share = static_cast<int64_t>(num / (2ull * Mt));
+        share = static_cast<int64_t>(udiv_small(num, 2ull * Mt));
       }
       int64_t q = s_floor[s] + share;
       if (q > s_len[s]) q = s_len[s];

@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 16 : (kEpt <= 8 ? 8 : 4))
   ss.b = reinterpret_cast<int32_t*>(smem + p.ly.off_b);
   ss.part = part;
   ss.pre = pre;
+  ss.sub = nullptr;
   ss.total = &total;
   ss.nseg = &nseg;
   unit::segment_phase<NT>(p.seg, u, mass_sm + pad, pad, n, ss, true);
