@@ -25,9 +25,9 @@ constexpr int kThreads = 256;  // units up to 4096 slots (see select_kernel)
 // Dynamic shared memory: start, want [S_max] | flags [T] | the radix
 // histograms [warps][256] of the picks, reused by the pick keys [budget] of the
 // excess search (units past kRegPer * kThreads slots; a barrier separates the
-// two uses).
+// two uses) | with 32 warps, the CTA-wide histogram [256 + 4] of that search.
 struct SelLayout {
-  int off_flag, off_key, off_hist, total;
+  int off_flag, off_key, off_hist, off_xhist, total;
 };
 __host__ __device__ inline SelLayout sel_layout(int S_max, int T, int budget, int warps) {
   SelLayout l;
@@ -37,6 +37,8 @@ __host__ __device__ inline SelLayout sel_layout(int S_max, int T, int budget, in
   const int keys = T > kRegPer * kThreads ? 4 * budget : 0;
   const int hist = 1024 * warps;
   l.total = l.off_key + (keys > hist ? keys : hist);
+  l.off_xhist = (l.total + 15) & ~15;
+  if (warps >= 32) l.total = l.off_xhist + 4 * (256 + 4);
   return l;
 }
 
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(NT, NT == kThreads ? 6 : 1)
   // [budget] pick keys of the excess search of long units (T > kRegPer * 256)
   ss.key = reinterpret_cast<uint32_t*>(sm + ly.off_key);
   ss.hist = reinterpret_cast<int*>(sm + ly.off_hist);         // [NT/32][256]
+  ss.xhist = NT >= 1024 ? reinterpret_cast<int*>(sm + ly.off_xhist) : nullptr;  // [256 + 4]
   ss.red = red;
   ss.red2 = red2;
   ss.scan = s_scan;

@@ -1158,6 +1158,65 @@ __device__ __forceinline__ void pick_segment_radix(const float* sc, uint8_t* fla
   __syncwarp();
 }
 
+// The k-th smallest (1-based, k <= n) of key[0, n) in shared memory, by all NT
+// threads of the CTA (barriers inside): a most-significant-digit radix select
+// over four 8-bit digits.  Each pass counts the keys that share the digits
+// fixed so far by their next digit (a 256-bin histogram in `hist`), and one
+// warp fixes the digit at which the count from the bottom reaches the rank
+// still wanted; hist[256], hist[257] pass the digit and the count below it to
+// every thread.
+template <int NT>
+__device__ __forceinline__ uint32_t cta_kth_smallest(const uint32_t* key, int n, int k,
+                                                     int* hist) {
+  uint32_t x = 0;
+  int need = k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += NT) hist[i] = 0;
+    __syncthreads();  // (also: every thread has read the last pass's digit)
+    const uint32_t above = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
+    for (int j = threadIdx.x; j < n; j += NT) {
+      const uint32_t kj = key[j];
+      if ((kj & above) == x) atomicAdd(&hist[(kj >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      // lane L takes bins 8L .. 8L+7, ascending
+      const int4 a = reinterpret_cast<const int4*>(hist)[2 * lane];
+      const int4 b = reinterpret_cast<const int4*>(hist)[2 * lane + 1];
+      const int c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      int s8 = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s8 += c[j];
+      int incl = s8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      int run = incl - s8, digit = 0, below = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool hit = run < need && run + c[j] >= need;
+        digit = hit ? 8 * lane + j : digit;
+        below = hit ? run : below;
+        run += c[j];
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, incl - s8 < need && need <= incl)) - 1;
+      digit = __shfl_sync(0xffffffffu, digit, src);
+      below = __shfl_sync(0xffffffffu, below, src);
+      if (lane == 0) {
+        hist[256] = digit;
+        hist[257] = below;
+      }
+    }
+    __syncthreads();
+    x |= static_cast<uint32_t>(hist[256]) << shift;
+    need -= hist[257];
+  }
+  return x;
+}
+
 // Where the selection reads the unit's segments: the global arrays written by
 // segment_phase (absolute starts) or its shared arrays (valid offsets).
 struct SegsGlobal {
@@ -1187,6 +1246,7 @@ struct SelSmem {
   uint8_t* flag;
   uint32_t* key;
   int* hist;  // [NT/32][256], 16-byte aligned: one radix histogram per warp
+  int* xhist;  // [256 + 4], 16-byte aligned: the excess search of 1024-thread CTAs
   int* red;
   int* red2;
   int* scan;
@@ -1268,7 +1328,8 @@ __device__ __forceinline__ void select_phase(const SelParams& p, int u, const fl
   if (excess > 0) {
     // x = the excess-th smallest pick key: largest x with #(pick key < x) < excess
     uint32_t x = 0;
-    if (per <= kRegPer) {  // CTA-uniform: every thread takes the same branch (barriers inside)
+    // CTA-uniform: every thread takes the same branch (barriers inside)
+    if (NT < 1024 && per <= kRegPer) {
       uint32_t key[kRegPer];
       bool pk[kRegPer];
 #pragma unroll
@@ -1314,7 +1375,11 @@ __device__ __forceinline__ void select_phase(const SelParams& p, int u, const fl
       for (int v = lo; v < hi; ++v)
         if (flag[v] == kPick) sm.key[pos++] = score_key<kLdg>(sc, v);
       __syncthreads();
-      if (n_pick <= kKeyPer * NT) {  // CTA-uniform
+      if constexpr (NT >= 1024) {
+        // many warps: four radix passes instead of 32 bitwise steps, each with
+        // a barrier across the CTA
+        x = cta_kth_smallest<NT>(sm.key, n_pick, excess, sm.xhist);
+      } else if (n_pick <= kKeyPer * NT) {  // CTA-uniform
         uint32_t key[kKeyPer];
 #pragma unroll
         for (int i = 0; i < kKeyPer; ++i) {
@@ -1377,27 +1442,61 @@ __device__ __forceinline__ void select_phase(const SelParams& p, int u, const fl
     __syncthreads();
   }
 
-  // ordered write-out: contiguous ranges per thread + block exclusive scan
-  int cnt = 0;
-  for (int v = lo; v < hi; ++v) cnt += flag[v] != kOut ? 1 : 0;
-  int incl = cnt;
+  if constexpr (NT >= 1024) {
+    // ordered write-out, coalesced: each warp takes a run of whole 32-slot
+    // groups, and a ballot places its kept slots, consecutive lanes at
+    // consecutive positions (one thread's run of positions would scatter a
+    // warp's stores over 32 places)
+    const int gpw = ((n + 31) / 32 + kWarps - 1) / kWarps;  // groups per warp
+    const int w_lo = min(n, warp * gpw * 32), w_hi = min(n, w_lo + gpw * 32);
+    int cnt = 0;
+    for (int b = w_lo; b < w_hi; b += 32) {
+      const int v = b + lane;
+      cnt += __popc(__ballot_sync(0xffffffffu, v < w_hi && flag[v] != kOut));
+    }
+    __syncthreads();  // scan may still be read by the excess pass
+    if (lane == 0) sm.scan[warp] = cnt;
+    __syncthreads();
+    int pos = 0, total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = sm.scan[w];
+      pos += w < warp ? c : 0;
+      total += c;
+    }
+    const uint32_t lower = (1u << lane) - 1u;
+    for (int b = w_lo; b < w_hi; b += 32) {
+      const int v = b + lane;
+      const bool keep = v < w_hi && flag[v] != kOut;
+      const uint32_t ball = __ballot_sync(0xffffffffu, keep);
+      const int at = pos + __popc(ball & lower);
+      if (keep && at < p.budget) out[at] = pad + v;
+      pos += __popc(ball);
+    }
+    for (int r = total + threadIdx.x; r < p.budget; r += NT) out[r] = -1;
+    if (threadIdx.x == 0) p.n_kept[u] = min(total, p.budget);
+  } else {
+    // ordered write-out: contiguous ranges per thread + block exclusive scan
+    int cnt = 0;
+    for (int v = lo; v < hi; ++v) cnt += flag[v] != kOut ? 1 : 0;
+    int incl = cnt;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    __syncthreads();  // scan may still be read by the excess pass
+    if (lane == 31) sm.scan[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += sm.scan[w];
+    int pos = wbase + incl - cnt;
+    for (int v = lo; v < hi; ++v)
+      if (flag[v] != kOut && pos < p.budget) out[pos++] = pad + v;
+    int total = 0;
+    for (int w = 0; w < kWarps; ++w) total += sm.scan[w];
+    for (int r = total + threadIdx.x; r < p.budget; r += NT) out[r] = -1;
+    if (threadIdx.x == 0) p.n_kept[u] = min(total, p.budget);
   }
-  __syncthreads();  // scan may still be read by the excess pass
-  if (lane == 31) sm.scan[warp] = incl;
-  __syncthreads();
-  int wbase = 0;
-  for (int w = 0; w < warp; ++w) wbase += sm.scan[w];
-  int pos = wbase + incl - cnt;
-  for (int v = lo; v < hi; ++v)
-    if (flag[v] != kOut && pos < p.budget) out[pos++] = pad + v;
-  int total = 0;
-  for (int w = 0; w < kWarps; ++w) total += sm.scan[w];
-  for (int r = total + threadIdx.x; r < p.budget; r += NT) out[r] = -1;
-  if (threadIdx.x == 0) p.n_kept[u] = min(total, p.budget);
 }
 
 }  // namespace unit

@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(NT, NT == 128 ? 16 : (kEpt <= 8 ? 8 : 4))
   sl.flag = A;
   sl.key = reinterpret_cast<uint32_t*>(A + p.ly.off_key);
   sl.hist = reinterpret_cast<int*>(A + p.ly.off_hist);
+  sl.xhist = nullptr;  // (1024-thread CTAs only)
   sl.red = sred;
   sl.red2 = sred2;
   sl.scan = sscan;
