@@ -80,18 +80,28 @@ __global__ void __launch_bounds__(NT)
   const int n_carry = min(max(p.n_carry[b], 0), T - pad);
   const int ra = p.avg_pool / 2, rm = p.max_pool / 2;
   const float inv_k = 1.0f / static_cast<float>(p.avg_pool);
+  const bool pools75 = ra == 2 && rm == 3;
   float tot = 0.f, cin_c = 0.f, up_c = 0.f;
   for (int i = threadIdx.x; i < T; i += NT) {
     if (i < pad) {
       score[i] = -INFINITY;
       continue;
     }
-    float mx = -INFINITY;
-    for (int t = max(pad, i - rm); t <= min(T - 1, i + rm); ++t) mx = fmaxf(mx, a[t]);
+    float mx, s;
+    if (pools75 && i - 3 >= pad && i + 3 < T) {  // interior slot, default pools: unrolled
+      const float w0 = a[i - 3], w1 = a[i - 2], w2 = a[i - 1], w3 = a[i], w4 = a[i + 1],
+                  w5 = a[i + 2], w6 = a[i + 3];
+      mx = fmaxf(fmaxf(fmaxf(w0, w1), fmaxf(w2, w3)), fmaxf(fmaxf(w4, w5), w6));
+      s = (((w1 + w2) + w3) + w4) + w5;  // the loop's order
+    } else {
+      mx = -INFINITY;
+      for (int t = max(pad, i - rm); t <= min(T - 1, i + rm); ++t) mx = fmaxf(mx, a[t]);
+      s = 0.f;
+      for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
+    }
     score[i] = mx;
-    float s = 0.f;
-    for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
     const float up = fmaxf(s * inv_k, 0.f) + p.eps;
+    mass[i] = up;  // kept for the second sweep, which overwrites it
     tot += up;
     if (i < pad + n_carry) {
       cin_c += cin[i];
@@ -110,9 +120,7 @@ __global__ void __launch_bounds__(NT)
   for (int i = threadIdx.x; i < T; i += NT) {
     float mu = 0.f, c = 0.f;
     if (i >= pad) {
-      float s = 0.f;
-      for (int t = max(pad, i - ra); t <= min(T - 1, i + ra); ++t) s += a[t];
-      const float m = (fmaxf(s * inv_k, 0.f) + p.eps) * inv_total;
+      const float m = mass[i] * inv_total;  // the first sweep's up
       c = (i < pad + n_carry) ? lam * cin[i] + (1.0f - lam) * m : m;
       const float cn = (c_total > 0.f) ? c * inv_ct : m;
       mu = beta * m + (1.0f - beta) * cn;
