@@ -1015,7 +1015,8 @@ __device__ __forceinline__ void segment_phase(const SegParams& p, int u, const f
 
 // ---------------------------------------------------------------- step 4: selection
 
-constexpr int kRegPer = 8;   // slots per thread up to which the excess search keeps keys in registers
+// slots per thread up to which the excess search keeps keys in registers
+constexpr int kRegPer = 8;
 constexpr int kKeyPer = 16;  // longer units: gathered pick keys per thread held in registers
 
 enum : uint8_t { kOut = 0, kMust = 1, kPick = 2 };

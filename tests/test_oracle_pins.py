@@ -508,7 +508,8 @@ def test_compaction_is_index_select(ref):
     ko, vo, co = ref.compact(p, k, v, c, kept, nk)
     for u in range(U):
         idx = torch.tensor(kept[u, :nk[u]], dtype=torch.long)
-        assert np.array_equal(ko[u, :nk[u]], torch.index_select(torch.tensor(k[u].astype(np.int32)), 0, idx).numpy())
-        assert np.array_equal(vo[u, :nk[u]], torch.index_select(torch.tensor(v[u].astype(np.int32)), 0, idx).numpy())
+        for got, src in ((ko, k), (vo, v)):
+            want = torch.index_select(torch.tensor(src[u].astype(np.int32)), 0, idx).numpy()
+            assert np.array_equal(got[u, :nk[u]], want)
         assert np.array_equal(co[u, :nk[u]], c[u, kept[u, :nk[u]]])
         assert not ko[u, nk[u]:].any() and not vo[u, nk[u]:].any() and not co[u, nk[u]:].any()
