@@ -237,20 +237,36 @@ def test_select_bit_exact(ref, oracle_runs, name, scores):
     assert np.array_equal(kept, kept_ref)
 
 
-def test_select_over_budget_long(ref):
+@pytest.mark.parametrize("T,budget", [(6000, 700), (8192, 900), (32768, 4096)])
+def test_select_over_budget_long(ref, T, budget):
     """Long cache, large recent suffix: must-keep overflows the last segments'
-    quotas and the global removal path runs."""
+    quotas and the global removal path runs (asserted on the oracle's
+    segments), on the wide CTAs of units past 4096 slots: at most 8 slots per
+    thread (6000, 8192) and 32 (32768)."""
     import eviction_gb300 as kvc
-    rng = np.random.default_rng(11)
-    B, H, T, budget = 2, 2, 6000, 700
+    rng = np.random.default_rng(11 + T)
+    B, H, n_recent = 2, 2, 300
     pads = np.array([0, 1234], np.int32)
     mass = _random_masses(rng, B * H, T, np.repeat(pads, H))
-    p = ref.RefParams(group=1, head_dim=64, window=8, budget=budget, n_recent=300)
+    p = ref.RefParams(group=1, head_dim=64, window=8, budget=budget, n_recent=n_recent)
     st, ln, qu, ns = ref.segment_quota(p, mass, np.repeat(pads, H))
+    over = 0
+    for u in range(B * H):  # picks past the budget, by the selection's own counting
+        n = T - int(pads[u // H])
+        Bk = min(budget, n)
+        n_s = min(4, Bk)
+        n_r = min(n_recent, Bk - n_s)
+        picks = 0
+        for s in range(ns[u]):
+            a, L = st[u, s] - pads[u // H], ln[u, s]
+            mk = max(0, min(a + L, n_s) - a) + max(0, a + L - max(a, n - n_r))
+            picks += max(0, min(qu[u, s] - mk, L - mk))
+        over += n_s + n_r + picks - Bk > 0
+    assert over > 0
     score = np.where(mass > 0, rng.random(mass.shape) * 3, -np.inf).astype(np.float32)
     score[mass > 0] = np.round(score[mass > 0], 1)  # ties
     kept_ref, nk_ref = ref.select(p, score, np.repeat(pads, H), st, ln, qu, ns)
-    h = kvc.Handle(kvc.Config(1, B, H, 1, 64, T, budget, window=8, n_recent=300))
+    h = kvc.Handle(kvc.Config(1, B, H, 1, 64, T, budget, window=8, n_recent=n_recent))
     kept, nk = gu.gpu_select(h, score, pads, T, st, ln, qu, ns)
     assert np.array_equal(nk, nk_ref) and np.array_equal(kept, kept_ref)
 
