@@ -383,6 +383,43 @@ def test_quota_invariants_and_apportionment(ref, seed):
         assert np.all(np.abs(q - ideal) < 1.0 + 1e-9)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_quota_correction_is_the_best_bids(ref, seed):
+    """Reading 10's correction, one unit at a time on the exact remainders, as a
+    sort.  Giving a segment one unit lowers its remainder by the mass total, so
+    the greedy picks are a merge of per-segment decreasing sequences.  When
+    short, the units taken are the best D of all bids rem_s - k*sum(M)
+    (k < L_s - q_s) by value, ties to the lower index.  When over, they are the
+    worst D of rem_s + k*sum(M) (k < q_s - q_min_s), ties to the higher index.
+    Tiny tie-heavy cases (masses from {0..3}, some all zero), exact integers."""
+    rng = np.random.default_rng(60 + seed)
+    for _ in range(300):
+        ns = int(rng.integers(1, 9))
+        L = rng.integers(1, 13, ns).astype(np.int32)
+        M = rng.integers(0, 4, ns).astype(np.uint64) * np.uint64(rng.choice([1, 7, 1 << 30]))
+        q_min = int(rng.choice([1, 2, 4]))
+        floor = np.minimum(q_min, L).astype(np.int64)
+        budget = int(rng.integers(int(floor.sum()), int(L.sum()) + 1))
+        Mt = int(M.sum())
+        t_rem = budget - int(floor.sum())
+        q0 = np.array([min(int(L[s]), int(floor[s]) + ((2 * t_rem * int(M[s]) + Mt) // (2 * Mt)
+                                                      if Mt > 0 else 0)) for s in range(ns)])
+        rem = [int(floor[s]) * Mt + t_rem * int(M[s]) - int(q0[s]) * Mt for s in range(ns)]
+        D = budget - int(q0.sum())
+        q = q0.copy()
+        if D > 0:
+            bids = [(rem[s] - k * Mt, s) for s in range(ns) for k in range(int(L[s] - q0[s]))]
+            bids.sort(key=lambda b: (-b[0], b[1]))
+            for _, s in bids[:D]:
+                q[s] += 1
+        elif D < 0:
+            bids = [(rem[s] + k * Mt, s) for s in range(ns) for k in range(int(q0[s] - floor[s]))]
+            bids.sort(key=lambda b: (b[0], -b[1]))
+            for _, s in bids[:-D]:
+                q[s] -= 1
+        assert list(ref.quotas(L, M, budget, q_min)) == list(q), (L, M, budget, q_min)
+
+
 def test_quota_infeasible_minimums(ref):
     """More segments than budget: the heaviest segments get their minimum, sum = budget."""
     L = np.full(10, 16, np.int32)
