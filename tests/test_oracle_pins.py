@@ -391,7 +391,9 @@ def test_quota_correction_is_the_best_bids(ref, seed):
     short, the units taken are the best D of all bids rem_s - k*sum(M)
     (k < L_s - q_s) by value, ties to the lower index.  When over, they are the
     worst D of rem_s + k*sum(M) (k < q_s - q_min_s), ties to the higher index.
-    Tiny tie-heavy cases (masses from {0..3}, some all zero), exact integers."""
+    A quarter of the cases have infeasible minimums, handed out by a stable sort
+    on descending mass.  Tiny tie-heavy cases (masses from {0..3}, some all
+    zero), exact integers."""
     rng = np.random.default_rng(60 + seed)
     for _ in range(300):
         ns = int(rng.integers(1, 9))
@@ -399,7 +401,18 @@ def test_quota_correction_is_the_best_bids(ref, seed):
         M = rng.integers(0, 4, ns).astype(np.uint64) * np.uint64(rng.choice([1, 7, 1 << 30]))
         q_min = int(rng.choice([1, 2, 4]))
         floor = np.minimum(q_min, L).astype(np.int64)
-        budget = int(rng.integers(int(floor.sum()), int(L.sum()) + 1))
+        if rng.random() < 0.25 and floor.sum() > 1:
+            # infeasible minimums: they go to the heaviest segments first (ties:
+            # lower index), a stable sort by descending mass, until the budget
+            # runs out
+            budget = int(rng.integers(1, int(floor.sum())))
+            left = budget
+            for s in sorted(range(ns), key=lambda i: -int(M[i])):
+                give = min(int(floor[s]), left)
+                floor[s] = give
+                left -= give
+        else:
+            budget = int(rng.integers(int(floor.sum()), int(L.sum()) + 1))
         Mt = int(M.sum())
         t_rem = budget - int(floor.sum())
         q0 = np.array([min(int(L[s]), int(floor[s]) + ((2 * t_rem * int(M[s]) + Mt) // (2 * Mt)
