@@ -300,6 +300,15 @@ def test_segmentation_golden(ref):
     assert list(b) == cases["merge"]["boundaries"]
     st, ln, M = ref.segments(m.astype(np.float32))
     assert list(st) == cases["merge"]["seg_start"] and list(ln) == cases["merge"]["seg_len"]
+    # merge before split
+    n = 400
+    m = np.full(n, 0.05 / 398)
+    m[9], m[269] = 0.15, 0.80
+    b, _ = ref.boundaries(m.astype(np.float32))
+    assert list(b) == cases["merge_then_split"]["boundaries"]
+    st, ln, M = ref.segments(m.astype(np.float32))
+    assert list(st) == cases["merge_then_split"]["seg_start"]
+    assert list(ln) == cases["merge_then_split"]["seg_len"]
     # uniform
     n = 997
     b, _ = ref.boundaries(np.full(n, 1.0 / n, np.float32))
